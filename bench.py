@@ -1,0 +1,361 @@
+"""Benchmark of the ring-attention hot path on GB300.
+
+One step = one simulated rank of the large video context (432,000 tokens =
+120 frames x 3,600 tokens, H = 4, d = 128, P = 8): the rank's 54,000 queries
+against all 8 KV blocks in ring order, computed as one per-step fp32 partial
+per ring step (one kernel launch over every (query tile pair, step) unit),
+then the online-softmax merge of the 8 partials into bf16 O and fp32 LSE
+(second launch).  Inputs are seeded synthetic bf16 N(0,1) tensors resident in
+HBM; K and V (884 MB) exceed L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle on
+a bounded sample of the same workload instead.  With --gpus N > 1 (torchrun)
+every rank runs an independent replica (the path has no data-parallel
+collective on one node here); value = all ranks' work / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ring-attention fwd TFLOPS (bf16) & % dense BF16 peak; lse_merge HBM GB/s"
+WORKLOAD = "c5"
+WORKLOAD_DESC = ("one simulated rank of a 432,000-token video context (120 frames x 3,600 "
+                 "tokens), H=4, d=128, P=8 contiguous, non-causal: 54,000 queries x 8 ring "
+                 "blocks of 54,000 keys as per-step fp32 partials + lse_merge")
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target seconds of oracle work for the cpu_baseline sample")
+    return ap.parse_args()
+
+
+def _dist_init(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return {"hbm_gbs": m["hbm_gbs"], "bf16_tflops": m["bf16_tflops"],
+                "bf16_tflops_sustained": m.get("bf16_tflops_sustained", m["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def _kernel_traffic(kernel_file, key):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "ring_attention_attn_gb300", "csrc", kernel_file)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    with open(path) as f:
+        t = json.load(f).get(key)
+    if not t:
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return t["dram_bytes_per_launch"] if t.get("source_sha256_16") == digest else None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ra_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _cpu_baseline(seconds_target, quick_rows=4):
+    """Time the fp64 oracle on sampled c5 query rows (host cores)."""
+    import numpy as np
+    import oracle
+    import synth
+    from ring_attention_attn_gb300 import accounting as acc
+
+    w = synth.WORKLOADS[WORKLOAD]
+    q, k, v = synth.make_qkv(w)
+    per_row_flops = 4 * w.d * w.S
+    # calibrate with a few rows, then size the sample to ~seconds_target
+    rows = oracle.flat_rows(w.B, w.H, w.L, synth.sample_rows(w, quick_rows))
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, rows=rows)
+    dt = time.perf_counter() - t0
+    per_head = int(max(quick_rows, min(512, quick_rows * seconds_target / max(dt, 1e-3))))
+    rows = oracle.flat_rows(w.B, w.H, w.L, synth.sample_rows(w, per_head))
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = per_row_flops * len(rows)
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"{per_head} query rows per head x {w.B * w.H} heads of {WORKLOAD} "
+                      f"(of {w.L}), all {w.S} keys, fp64; {dt:.2f} s",
+            "seconds": dt, "full_workload_seconds_extrapolated":
+                dt * (w.B * w.H * w.L) / len(rows)}
+
+
+def run_reference(a, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    import synth
+
+    w = synth.WORKLOADS[WORKLOAD]
+    q, k, v = synth.make_qkv(w)
+    per_head = 24  # rows per head per step: ~27 GFLOP of fp64 per step
+    all_rows = synth.sample_rows(w, per_head * (a.steps + a.warmup))
+    flops_row = 4 * w.d * w.S
+    times = []
+    for i in range(a.warmup + a.steps):
+        sel = all_rows[i * per_head:(i + 1) * per_head]
+        rows = oracle.flat_rows(w.B, w.H, w.L, sel)
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, rows=rows)
+        if i >= a.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    flops = flops_row * per_head * w.B * w.H * a.steps
+    value = flops / total / 1e12
+    sample = (f"{per_head} query rows per head x {w.B * w.H} heads per step (of {w.L}), all "
+              f"{w.S} keys, fp64 oracle on host cores")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+            "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": 1e3 * total / a.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "B": w.B, "H": w.H, "S": w.S, "d": w.d,
+                       "P": w.P, "rank": 0, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(a, rank, world, local):
+    import torch
+
+    import synth
+    import ring_attention_attn_gb300 as ra
+    from ring_attention_attn_gb300 import accounting as acc
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[WORKLOAD]
+    q, k, v = synth.make_qkv(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    n = w.P
+    parts = torch.empty((n, w.B, w.H, w.L, w.d), dtype=torch.float32, device=dev)
+    lparts = torch.empty((n, w.B, w.H, w.L), dtype=torch.float32, device=dev)
+    out = torch.empty((w.B, w.H, w.L, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ra.ring_attn_fwd_rank(qd, kd, vd, w.P, 0, out_fp32=True, out=parts, lse=lparts,
+                              stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ra.lse_merge(parts, lparts, out=out, lse_out=lse, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ra.ra_get_status() != 0:
+        raise RuntimeError("device watchdog fired during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
+    clocks = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(a.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    if dist is not None:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    merge_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    status = ra.ra_get_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    flops = acc.attention_flops(w.B * w.H, w.L, w.S, w.d)
+    merge_bytes = acc.merge_bytes(n, w.B * w.H * w.L, w.d)
+    value = world * flops * a.steps / (total_ms * 1e-3) / 1e12
+    peaks = _peaks()
+    attn_avg = statistics.mean(attn_ms)
+    merge_avg = statistics.mean(merge_ms)
+    attn_tflops = flops / (attn_avg * 1e-3) / 1e12
+    merge_gbs = merge_bytes / (merge_avg * 1e-3) / 1e9
+    peak_t = peaks["bf16_tflops_sustained"]
+
+    # End to end through the public API with host buffers: pinned inputs
+    # copied in and the result copied out inside the timed region.
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e2e_steps = max(1, min(a.steps, 5))
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        step()
+        oh.copy_(out, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    h2d = (q.numel() + k.numel() + v.numel()) * 2
+    d2h = out.numel() * 2 + lse.numel() * 4
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cpu = _cpu_baseline(a.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": total_ms / a.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "B": w.B, "H": w.H, "S": w.S, "d": w.d,
+                       "P": w.P, "rank": 0, "seq_len": w.S, "global_batch": w.B,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (K+V 884.7 MB per replica)"},
+            "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak_t,
+                         "unit": "TFLOP/s", "frac": attn_tflops / peak_t,
+                         "traffic": _kernel_traffic("attn_fwd.cu", "ring_attn_kernel"),
+                         "kernel": "ring_attn_kernel<128, fp32 partials>",
+                         "peak_kind": f"bf16_tflops_sustained ({peaks['source']})"},
+            "merge": {"kernel": "lse_merge_kernel<128>", "bound": "hbm", "achieved": merge_gbs,
+                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": merge_gbs / peaks["hbm_gbs"], "bytes_per_launch": merge_bytes,
+                      "ms": merge_avg,
+                      "traffic": _kernel_traffic("merge.cu", "lse_merge_kernel")},
+            "kernel_ms": {"ring_attn": attn_avg, "lse_merge": merge_avg},
+            "attn_frac_of_burst_peak": attn_tflops / peaks["bf16_tflops"],
+            "clocks": clock_info,
+            "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "ms_per_step": e2e_ms / e2e_steps},
+            "gpu_launches": 2 * a.steps,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    a = _args()
+    rank, world, local = _dist_init(a.gpus)
+    if a.impl == "reference":
+        run_reference(a, rank, world)
+        return
+    run_ours(a, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,156 @@
+/*
+ * ringattn.h -- C ABI of the GB300 (sm_103a) ring-attention hot path.
+ *
+ * Ring attention for context parallelism: every one of P ranks keeps its
+ * chunk of queries and visits the P key/value blocks in ring order, folding
+ * each block's partial attention into a running result with the online
+ * softmax ("day 83" blog, "Context parallelism: splitting the sequence";
+ * k8ai "Sequence and Context Parallel", "How context parallel works").  Here
+ * the P ranks are P sequence chunks of one tensor on one GPU: a ring step is a
+ * change of key/value block, not a transfer.
+ *
+ * Conventions shared by every entry point
+ *  - Element types: bf16 (raw 16-bit storage, passed as void*), fp32 (float*).
+ *  - Layout [B, H, S, d], row-major, d innermost, contiguous.  d is 64 or 128.
+ *  - "Sharded order": rows [r*L, (r+1)*L) of each (b, h) hold rank r's chunk,
+ *    L = S / P, in the layout chosen by ra_cp_shard (contiguous, or zigzag
+ *    when causal).  Attention inputs and outputs are in sharded order.
+ *  - Softmax scale 1/sqrt(d); LSE = natural log of the row's sum of
+ *    exp(score), scale included.
+ *  - Every device pointer must be 16-byte aligned.  The caller owns all
+ *    memory; the library allocates no device memory.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *    default stream) and never synchronise, except ra_get_status.
+ *  - Return value: RA_OK (0) or a negative RA_ERR_* code.  Argument errors are
+ *    detected on the host before anything is launched.  A sizes product of
+ *    zero (B*H == 0 or S == 0) is a successful no-op.
+ */
+#ifndef RINGATTN_H
+#define RINGATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RA_OK 0
+#define RA_ERR_ARG (-1)     /* null pointer, negative size, bad enum value        */
+#define RA_ERR_SHAPE (-2)   /* S % P != 0, S % 2P != 0 for zigzag, d not 64/128   */
+#define RA_ERR_ALIGN (-3)   /* a device pointer is not 16-byte aligned            */
+#define RA_ERR_CUDA (-4)    /* a CUDA call or launch failed: see ra_last_cuda_error */
+#define RA_ERR_TIMEOUT (-5) /* a kernel's bounded wait expired (device watchdog)   */
+#define RA_ERR_WORKSPACE (-6) /* workspace missing or smaller than required        */
+
+#define RA_LAYOUT_CONTIGUOUS 0
+#define RA_LAYOUT_ZIGZAG 1
+
+/* Global <-> sharded token index maps (host only, no CUDA).
+ * Contiguous ("day 83" blog, "Context parallelism: splitting the sequence"):
+ *   rank r holds tokens [r*L, (r+1)*L).
+ * Zigzag, the balanced causal split (k8ai "How context parallel works"): the
+ *   sequence is cut into 2P chunks of C = S/(2P); rank r holds chunk r then
+ *   chunk 2P-1-r.  Sharded row j = r*L + i maps to global token
+ *   g = r*C + i (i < C) or (2P-1-r)*C + (i - C) (i >= C).
+ * s2g[j] = g and g2s[g] = j, both int64 arrays of S entries owned by the
+ * caller (either may be NULL).  Errors: RA_ERR_ARG, RA_ERR_SHAPE. */
+int ra_cp_shard_index(int64_t S, int P, int layout, int64_t *s2g, int64_t *g2s);
+
+/* KV block that rank r holds at ring step s: (r - s) mod P (k8ai ring
+ * diagram: at step 1 GPU0 gets K/V3, GPU1 gets K/V0).  Host only.  Returns -1
+ * on bad arguments. */
+int ra_ring_source(int P, int rank, int step);
+
+/* Row permutation of a bf16 [BH, S, d] tensor between global and sharded
+ * order under the map above: inverse = 0 writes y[j] = x[s2g[j]] (shard),
+ * inverse = 1 writes y[g] = x[g2s[g]] (unshard).  x and y must not overlap.
+ * Bit-exact copy; 128-bit coalesced loads and stores. */
+int ra_cp_shard(const void *x, void *y, int64_t BH, int64_t S, int d, int P, int layout,
+                int inverse, void *stream);
+
+/* Frame transpose of a video tensor ("day 83" blog, "The spatial-temporal
+ * twist": tokens t*N + n).  bf16 rows of d elements: inverse = 0 maps
+ * [BH, T, N, d] -> [BH, N, T, d]; inverse = 1 maps back.  x, y must not
+ * overlap. */
+int ra_frame_transpose(const void *x, void *y, int64_t BH, int64_t T, int64_t N, int d,
+                       int inverse, void *stream);
+
+/* Ring attention forward for all P simulated ranks.
+ * q, k, v: bf16 [B, H, S, d] in sharded order (contiguous layout when
+ * causal = 0, zigzag when causal = 1).  out: bf16 [B, H, S, d], lse: fp32
+ * [B, H, S], both in sharded order.  Rank r's queries visit KV blocks
+ * (r - s) mod P for s = 0..P-1; scores are masked by global token position
+ * (key <= query) when causal.  Requires S % P == 0 (S % 2P == 0 if causal).
+ * Result equals full attention ("mathematically equivalent to full-sequence
+ * attention", ultralytics glossary, "How Context Parallelism Works"). */
+int ring_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                  int H, int64_t S, int d, int P, int causal, void *stream);
+
+/* One rank's share of the ring, for a range of ring steps.
+ * q_local: bf16 [B, H, L, d], rank `rank`'s queries (L = S/P); k, v: bf16
+ * [B, H, S, d] in sharded order.  Steps step_begin <= s < step_end visit
+ * blocks (rank - s) mod P.
+ *  out_fp32 = 0: out_local bf16 [B, H, L, d] and lse_local fp32 [B, H, L]
+ *                hold attention over the keys of those steps (normalised).
+ *  out_fp32 = 1: one partial per step, n = step_end - step_begin:
+ *                out_local fp32 [n, B, H, L, d] (normalised per step) and
+ *                lse_local fp32 [n, B, H, L]; a row that sees no key in a step
+ *                gets O = 0, LSE = -inf.  Merge them with lse_merge.
+ * Errors: RA_ERR_ARG if the step range is empty or outside [0, P], or rank is
+ * outside [0, P). */
+int ring_attn_fwd_rank(const void *q_local, const void *k, const void *v, void *out_local,
+                       float *lse_local, int B, int H, int64_t S, int d, int P, int rank,
+                       int causal, int step_begin, int step_end, int out_fp32, void *stream);
+
+/* Online-softmax merge of n normalised partials of the same rows ("the online
+ * softmax trick", "day 83" blog, "Context parallelism: splitting the
+ * sequence"):  M = max_i LSE_i,  w_i = exp(LSE_i - M),
+ *   LSE = M + ln(sum w_i),  O = sum w_i O_i / sum w_i;
+ * rows whose partials are all empty (LSE = -inf) get O = 0, LSE = -inf.
+ * o_parts fp32 [n][rows][d], lse_parts fp32 [n][rows]; out bf16 [rows][d],
+ * lse_out fp32 [rows].  1 <= n <= 64. */
+int lse_merge(const float *o_parts, const float *lse_parts, int n, int64_t rows, int d,
+              void *out, float *lse_out, void *stream);
+
+/* Factored video attention ("day 83" blog, "The spatial-temporal twist").
+ * q, k, v: bf16 [B, H, T*N, d], token t*N + n (whole frames contiguous).
+ *  spatial:  out_s bf16 [B, H, T*N, d], lse_s fp32 [B, H, T*N]: attention of
+ *            each token over the N tokens of its own frame.
+ *  temporal: out_t bf16 [B, H, T*N, d], lse_t fp32 [B, H, T*N]: attention of
+ *            each token over the T tokens at its spatial position, run as a
+ *            ring over P chunks of T/P frames (T % P == 0).
+ * The two outputs are independent (not chained).  workspace: device memory
+ * of at least factored_attn_workspace(...) bytes, 256-byte aligned, owned
+ * by the caller and used as scratch by this call only. */
+int factored_attn(const void *q, const void *k, const void *v, void *out_s, float *lse_s,
+                  void *out_t, float *lse_t, int B, int H, int T, int N, int d, int P,
+                  void *workspace, size_t ws_bytes, void *stream);
+
+/* Scratch bytes factored_attn needs for these sizes (0 on bad arguments). */
+size_t factored_attn_workspace(int B, int H, int T, int N, int d);
+
+/* Synchronises `stream`, then returns and clears the device status word:
+ * RA_OK, or RA_ERR_TIMEOUT if a kernel's bounded wait expired since the last
+ * call (the kernel then stopped early and its outputs are undefined), or
+ * RA_ERR_CUDA if the synchronisation failed. */
+int ra_get_status(void *stream);
+
+/* Bounded-wait limit of the kernels' barrier waits, in nanoseconds (default
+ * 2e9).  Values <= 0 restore the default.  Applies to later launches. */
+void ra_set_watchdog_ns(int64_t ns);
+
+/* Runs a kernel whose only wait can never be satisfied, with the current
+ * watchdog limit, to exercise the timeout path: returns RA_OK when launched;
+ * ra_get_status then reports RA_ERR_TIMEOUT. */
+int ra_watchdog_selftest(void *stream);
+
+/* Text for an RA_* code; the last CUDA error (cudaError_t) seen on RA_ERR_CUDA. */
+const char *ra_strerror(int code);
+int ra_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RINGATTN_H */

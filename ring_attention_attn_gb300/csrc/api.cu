@@ -1,0 +1,336 @@
+// C ABI of the ring-attention library: argument validation, the device
+// status word, and the launch of each entry point on the caller's stream.
+// Declarations and the contract of every function are in include/ringattn.h.
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "ra_internal.h"
+#include "ringattn.h"
+
+namespace {
+
+__device__ int g_status;  // first device-side error since the last ra_get_status
+
+std::atomic<int> g_last_cuda_error{0};
+std::atomic<int64_t> g_watchdog_ns{2000000000LL};
+
+int fail_cuda(cudaError_t e) {
+  g_last_cuda_error.store(static_cast<int>(e));
+  return RA_ERR_CUDA;
+}
+
+int *status_ptr() {
+  static int *ptrs[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int *>(p);
+  }
+  return ptrs[dev];
+}
+
+bool watchdog(ra::WatchdogParams *wd) {
+  wd->status = status_ptr();
+  wd->limit_ns = g_watchdog_ns.load();
+  return wd->status != nullptr;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+float scale_log2(int d) { return static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(d))); }
+
+int check_d(int d) { return (d == 64 || d == 128) ? RA_OK : RA_ERR_SHAPE; }
+
+// Largest row count a 2-D tensor map coordinate can address with a tile of
+// slack past the end.
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 512;
+
+}  // namespace
+
+extern "C" {
+
+const char *ra_strerror(int code) {
+  switch (code) {
+    case RA_OK: return "ok";
+    case RA_ERR_ARG: return "invalid argument (null pointer, negative size or bad option)";
+    case RA_ERR_SHAPE: return "unsupported shape (S % P, S % 2P for zigzag, or d not 64/128)";
+    case RA_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case RA_ERR_CUDA: return "CUDA error (see ra_last_cuda_error)";
+    case RA_ERR_TIMEOUT: return "device watchdog: a kernel's bounded wait expired";
+    case RA_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown error";
+  }
+}
+
+int ra_last_cuda_error(void) { return g_last_cuda_error.load(); }
+
+void ra_set_watchdog_ns(int64_t ns) { g_watchdog_ns.store(ns > 0 ? ns : 2000000000LL); }
+
+int ra_cp_shard_index(int64_t S, int P, int layout, int64_t *s2g, int64_t *g2s) {
+  if (S < 0 || P <= 0 || (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG))
+    return RA_ERR_ARG;
+  if (S % P != 0) return RA_ERR_SHAPE;
+  if (layout == RA_LAYOUT_ZIGZAG && S % (2 * static_cast<int64_t>(P)) != 0) return RA_ERR_SHAPE;
+  const int64_t L = S / P;
+  const int64_t C = L / 2;
+  for (int64_t j = 0; j < S; ++j) {
+    const int64_t r = j / L, i = j % L;
+    int64_t g = j;
+    if (layout == RA_LAYOUT_ZIGZAG) g = i < C ? r * C + i : (2 * P - 1 - r) * C + (i - C);
+    if (s2g) s2g[j] = g;
+    if (g2s) g2s[g] = j;
+  }
+  return RA_OK;
+}
+
+int ra_ring_source(int P, int rank, int step) {
+  if (P <= 0 || rank < 0 || rank >= P || step < 0) return -1;
+  return ((rank - step) % P + P) % P;
+}
+
+int ra_cp_shard(const void *x, void *y, int64_t BH, int64_t S, int d, int P, int layout,
+                int inverse, void *stream) {
+  if (BH < 0 || S < 0 || P <= 0 || (inverse != 0 && inverse != 1) ||
+      (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG))
+    return RA_ERR_ARG;
+  if (check_d(d) != RA_OK || S % P != 0) return RA_ERR_SHAPE;
+  if (layout == RA_LAYOUT_ZIGZAG && S % (2 * static_cast<int64_t>(P)) != 0) return RA_ERR_SHAPE;
+  if (BH == 0 || S == 0) return RA_OK;
+  if (!x || !y) return RA_ERR_ARG;
+  if (!aligned16(x) || !aligned16(y)) return RA_ERR_ALIGN;
+  cudaError_t e = ra::launch_row_permute(x, y, BH, S, d * 2, inverse ? 1 : 0, P, 0, layout,
+                                         as_stream(stream));
+  return e == cudaSuccess ? RA_OK : fail_cuda(e);
+}
+
+int ra_frame_transpose(const void *x, void *y, int64_t BH, int64_t T, int64_t N, int d,
+                       int inverse, void *stream) {
+  if (BH < 0 || T < 0 || N < 0 || (inverse != 0 && inverse != 1)) return RA_ERR_ARG;
+  if (check_d(d) != RA_OK) return RA_ERR_SHAPE;
+  if (BH == 0 || T == 0 || N == 0) return RA_OK;
+  if (!x || !y) return RA_ERR_ARG;
+  if (!aligned16(x) || !aligned16(y)) return RA_ERR_ALIGN;
+  cudaError_t e = ra::launch_row_permute(x, y, BH, T * N, d * 2, inverse ? 3 : 2, T, N, 0,
+                                         as_stream(stream));
+  return e == cudaSuccess ? RA_OK : fail_cuda(e);
+}
+
+int ring_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                  int H, int64_t S, int d, int P, int causal, void *stream) {
+  if (B < 0 || H < 0 || S < 0 || P <= 0 || (causal != 0 && causal != 1)) return RA_ERR_ARG;
+  if (check_d(d) != RA_OK || S % P != 0) return RA_ERR_SHAPE;
+  if (causal && S % (2 * static_cast<int64_t>(P)) != 0) return RA_ERR_SHAPE;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH == 0 || S == 0) return RA_OK;
+  if (!q || !k || !v || !out || !lse) return RA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return RA_ERR_ALIGN;
+  if (BH * S > kMaxRows || BH > 0x7fffffff) return RA_ERR_SHAPE;
+  ra::AttnParams p{};
+  const int64_t L = S / P;
+  p.BH = static_cast<int>(BH);
+  p.G = 1;
+  p.n_ranks = P;
+  p.n_stepgroups = 1;
+  p.n_pairs = static_cast<int>((L + 255) / 256);
+  p.q_rows_bh = S;
+  p.kv_rows_bh = S;
+  p.L = L;
+  p.P = P;
+  p.rank_begin = 0;
+  p.step_begin = 0;
+  p.steps_per_group = P;
+  p.causal = causal;
+  p.scale_log2 = scale_log2(d);
+  p.out = out;
+  p.lse = lse;
+  if (!watchdog(&p.wd)) return fail_cuda(cudaGetLastError());
+  cudaError_t e = ra::launch_ring_attn(q, BH * S, k, v, BH * S, d, false, p, as_stream(stream));
+  return e == cudaSuccess ? RA_OK : fail_cuda(e);
+}
+
+int ring_attn_fwd_rank(const void *q_local, const void *k, const void *v, void *out_local,
+                       float *lse_local, int B, int H, int64_t S, int d, int P, int rank,
+                       int causal, int step_begin, int step_end, int out_fp32, void *stream) {
+  if (B < 0 || H < 0 || S < 0 || P <= 0 || (causal != 0 && causal != 1) ||
+      (out_fp32 != 0 && out_fp32 != 1))
+    return RA_ERR_ARG;
+  if (rank < 0 || rank >= P || step_begin < 0 || step_end > P || step_begin >= step_end)
+    return RA_ERR_ARG;
+  if (check_d(d) != RA_OK || S % P != 0) return RA_ERR_SHAPE;
+  if (causal && S % (2 * static_cast<int64_t>(P)) != 0) return RA_ERR_SHAPE;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH == 0 || S == 0) return RA_OK;
+  if (!q_local || !k || !v || !out_local || !lse_local) return RA_ERR_ARG;
+  if (!aligned16(q_local) || !aligned16(k) || !aligned16(v) || !aligned16(out_local) ||
+      !aligned16(lse_local))
+    return RA_ERR_ALIGN;
+  if (BH * S > kMaxRows || BH > 0x7fffffff) return RA_ERR_SHAPE;
+  const int64_t L = S / P;
+  const int n = step_end - step_begin;
+  ra::AttnParams p{};
+  p.BH = static_cast<int>(BH);
+  p.G = 1;
+  p.n_ranks = 1;
+  p.n_pairs = static_cast<int>((L + 255) / 256);
+  p.q_rows_bh = L;
+  p.kv_rows_bh = S;
+  p.L = L;
+  p.P = P;
+  p.rank_begin = rank;
+  p.step_begin = step_begin;
+  if (out_fp32) {
+    p.n_stepgroups = n;
+    p.steps_per_group = 1;
+    p.out_part_stride = BH * L * d;
+    p.lse_part_stride = BH * L;
+  } else {
+    p.n_stepgroups = 1;
+    p.steps_per_group = n;
+  }
+  p.causal = causal;
+  p.scale_log2 = scale_log2(d);
+  p.out = out_local;
+  p.lse = lse_local;
+  if (!watchdog(&p.wd)) return fail_cuda(cudaGetLastError());
+  cudaError_t e =
+      ra::launch_ring_attn(q_local, BH * L, k, v, BH * S, d, out_fp32 != 0, p, as_stream(stream));
+  return e == cudaSuccess ? RA_OK : fail_cuda(e);
+}
+
+int lse_merge(const float *o_parts, const float *lse_parts, int n, int64_t rows, int d, void *out,
+              float *lse_out, void *stream) {
+  if (n < 1 || n > 64 || rows < 0) return RA_ERR_ARG;
+  if (check_d(d) != RA_OK) return RA_ERR_SHAPE;
+  if (rows == 0) return RA_OK;
+  if (!o_parts || !lse_parts || !out || !lse_out) return RA_ERR_ARG;
+  if (!aligned16(o_parts) || !aligned16(out) || !aligned16(lse_parts) || !aligned16(lse_out))
+    return RA_ERR_ALIGN;
+  cudaError_t e = ra::launch_lse_merge(o_parts, lse_parts, n, rows, d, out, lse_out,
+                                       as_stream(stream));
+  return e == cudaSuccess ? RA_OK : fail_cuda(e);
+}
+
+// Workspace of factored_attn: the frame-transposed q, k, v, the temporal
+// output in transposed order (bf16) and its LSE (fp32), each 256-byte aligned.
+static size_t ws_part(size_t bytes) { return (bytes + 255) & ~static_cast<size_t>(255); }
+
+size_t factored_attn_workspace(int B, int H, int T, int N, int d) {
+  if (B < 0 || H < 0 || T < 0 || N < 0 || check_d(d) != RA_OK) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * T * N;
+  return 4 * ws_part(rows * d * 2) + ws_part(rows * 4);
+}
+
+int factored_attn(const void *q, const void *k, const void *v, void *out_s, float *lse_s,
+                  void *out_t, float *lse_t, int B, int H, int T, int N, int d, int P,
+                  void *workspace, size_t ws_bytes, void *stream) {
+  if (B < 0 || H < 0 || T < 0 || N < 0 || P <= 0) return RA_ERR_ARG;
+  if (check_d(d) != RA_OK || T % P != 0) return RA_ERR_SHAPE;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t S = static_cast<int64_t>(T) * N;
+  if (BH == 0 || S == 0) return RA_OK;
+  if (!q || !k || !v || !out_s || !lse_s || !out_t || !lse_t) return RA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out_s) || !aligned16(lse_s) ||
+      !aligned16(out_t) || !aligned16(lse_t))
+    return RA_ERR_ALIGN;
+  if (BH * S > kMaxRows || BH > 0x7fffffff) return RA_ERR_SHAPE;
+  const size_t need = factored_attn_workspace(B, H, T, N, d);
+  if (!workspace || ws_bytes < need) return RA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RA_ERR_ALIGN;
+  cudaStream_t st = as_stream(stream);
+  ra::WatchdogParams wd;
+  if (!watchdog(&wd)) return fail_cuda(cudaGetLastError());
+  cudaError_t e;
+
+  // Spatial: T independent N-token problems per (b, h), no ring.
+  {
+    ra::AttnParams p{};
+    p.BH = static_cast<int>(BH);
+    p.G = T;
+    p.n_ranks = 1;
+    p.n_stepgroups = 1;
+    p.n_pairs = (N + 255) / 256;
+    p.q_rows_bh = S;
+    p.q_rows_g = N;
+    p.kv_rows_bh = S;
+    p.kv_rows_g = N;
+    p.L = N;
+    p.P = 1;
+    p.steps_per_group = 1;
+    p.scale_log2 = scale_log2(d);
+    p.out = out_s;
+    p.lse = lse_s;
+    p.wd = wd;
+    e = ra::launch_ring_attn(q, BH * S, k, v, BH * S, d, false, p, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  // Temporal: transpose to [N, T] order, then N problems of T tokens per
+  // (b, h), each a ring over P chunks of T/P frames; transpose back.
+  const size_t tbytes = ws_part(static_cast<size_t>(BH * S) * d * 2);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  void *qT = ws, *kT = ws + tbytes, *vT = ws + 2 * tbytes, *oT = ws + 3 * tbytes;
+  float *lT = reinterpret_cast<float *>(ws + 4 * tbytes);
+  const void *src[3] = {q, k, v};
+  void *dst[3] = {qT, kT, vT};
+  for (int i = 0; i < 3; ++i) {
+    e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 2, T, N, 0, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  {
+    ra::AttnParams p{};
+    const int64_t L = T / P;
+    p.BH = static_cast<int>(BH);
+    p.G = N;
+    p.n_ranks = P;
+    p.n_stepgroups = 1;
+    p.n_pairs = static_cast<int>((L + 255) / 256);
+    p.q_rows_bh = S;
+    p.q_rows_g = T;
+    p.kv_rows_bh = S;
+    p.kv_rows_g = T;
+    p.L = L;
+    p.P = P;
+    p.steps_per_group = P;
+    p.scale_log2 = scale_log2(d);
+    p.out = oT;
+    p.lse = lT;
+    p.wd = wd;
+    e = ra::launch_ring_attn(qT, BH * S, kT, vT, BH * S, d, false, p, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  e = ra::launch_row_permute(oT, out_t, BH, S, d * 2, 3, T, N, 0, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = ra::launch_row_permute(lT, lse_t, BH, S, 4, 3, T, N, 0, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return RA_OK;
+}
+
+int ra_get_status(void *stream) {
+  cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_status, sizeof(int));
+  if (e != cudaSuccess) return fail_cuda(e);
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return v;
+}
+
+int ra_watchdog_selftest(void *stream) {
+  ra::WatchdogParams wd;
+  if (!watchdog(&wd)) return fail_cuda(cudaGetLastError());
+  cudaError_t e = ra::launch_watchdog_selftest(wd, as_stream(stream));
+  return e == cudaSuccess ? RA_OK : fail_cuda(e);
+}
+
+}  // extern "C"

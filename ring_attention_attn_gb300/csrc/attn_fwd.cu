@@ -1,0 +1,598 @@
+// Blockwise ring-attention forward for sm_103a (GB300): TMA -> tcgen05 MMA
+// into tensor memory -> online softmax in registers -> tcgen05 MMA -> epilogue.
+//
+// What it computes (k8ai "Sequence and Context Parallel", "How context
+// parallel works"; "day 83" blog, "Context parallelism: splitting the
+// sequence"): rank r's queries attend to the key/value blocks (r - s) mod P of
+// its ring steps s, one 128-key tile at a time, folding every tile into a
+// running row max m, row sum l and output O with the online softmax
+//     m' = max(m, max_j s_j),  O = e^(m - m') O + sum_j e^(s_j - m') v_j,
+//     l = e^(m - m') l + sum_j e^(s_j - m'),
+// and finally writes O / l and LSE = m + ln l.  Scores are q.k / sqrt(d),
+// masked by global token position (key <= query) for the zigzag causal split.
+//
+// CTA structure (384 threads, one CTA per SM, 230 KB shared memory):
+//   warp 0       TMA producer: Q tile pair once, then K_j, V_j tiles through a
+//                ring of shared-memory slots (mbarrier full/empty pairs).
+//   warp 1       allocates 512 TMEM columns; one thread issues every
+//                tcgen05.mma and tcgen05.commit.
+//   warps 4..7   softmax for query tile 0 (one thread per query row),
+//   warps 8..11  softmax for query tile 1; the two tiles ping-pong so the
+//                tensor core computes one tile's QK^T / PV while the other
+//                tile's softmax runs.
+// Tensor memory: S0 cols [0,128), S1 [128,256), O0 [256,256+d), O1 [384,384+d).
+// P (bf16 probabilities) goes through shared memory in the 128-byte-swizzled
+// K-major layout the MMA reads, so both MMAs take their operands from SMEM.
+//
+// The O rescale is lazy: a row's reference max only moves when the new max
+// exceeds it by more than 2^8 (in exp2 units), so P entries stay <= 256 and
+// the O accumulator in TMEM is touched only on such rare jumps.
+#include <math.h>
+
+#include "ra_device.cuh"
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kBM = 128;  // query rows per tile
+constexpr int kBN = 128;  // keys per tile
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int D>
+struct Cfg {
+  static constexpr int kChunks = D / 64;         // 128-byte swizzle atoms along d
+  static constexpr int kChunkBytes = 128 * 128;  // one atom column of a 128-row tile
+  static constexpr int kQTile = kBM * D * 2;
+  static constexpr int kKVTile = kBN * D * 2;
+  static constexpr int kPTile = kBM * kBN * 2;
+  static constexpr int kSlots = (D == 128) ? 3 : 8;
+  static constexpr int kOffQ0 = 0;
+  static constexpr int kOffQ1 = kQTile;
+  static constexpr int kOffP0 = 2 * kQTile;
+  static constexpr int kOffP1 = 2 * kQTile + kPTile;
+  static constexpr int kOffKV = 2 * kQTile + 2 * kPTile;
+  static constexpr int kOffBar = kOffKV + kSlots * kKVTile;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+};
+
+// Barrier indices (8 bytes each) in the barrier block.
+enum : int {
+  kBarQFull = 0,
+  kBarSFull = 1,   // +wg
+  kBarPFull = 3,   // +wg
+  kBarODone = 5,   // +wg
+  kBarDrain = 7,
+  kBarKVFull = 8,  // +slot; kv_empty follows the kv_full block
+};
+constexpr int kTmemSlotOff = 240;
+constexpr int kAbortOff = 244;
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns of S_i and O_i.
+__device__ __forceinline__ uint32_t col_s(int i) { return static_cast<uint32_t>(i) * 128u; }
+__device__ __forceinline__ uint32_t col_o(int i) { return 256u + static_cast<uint32_t>(i) * 128u; }
+
+__device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+// Global token position of local row i of rank `rank`'s chunk (zigzag: the
+// chunk is global chunks rank and 2P-1-rank, each C = L/2 rows).
+__device__ __forceinline__ int64_t zz_pos(int rank, int64_t i, int64_t C, int P) {
+  return i < C ? static_cast<int64_t>(rank) * C + i
+               : static_cast<int64_t>(2 * P - 1 - rank) * C + (i - C);
+}
+
+// Number of keys of tile [k0, k0+128) of block `src` that query position gq
+// may see.  Global key positions increase with the local index, so the
+// visible keys are a prefix of the tile.
+__device__ __forceinline__ int causal_visible(int src, int64_t k0, int64_t gq, int64_t L, int P) {
+  const int64_t C = L >> 1;
+  const int64_t n = min64(kBN, L - k0);
+  const int64_t endA = min64(k0 + n, C);
+  const int64_t lenA = max64(0, endA - k0);
+  const int64_t cntA = min64(lenA, max64(0, gq - (static_cast<int64_t>(src) * C + k0) + 1));
+  const int64_t startB = max64(k0, C);
+  const int64_t lenB = max64(0, k0 + n - startB);
+  const int64_t gB0 = static_cast<int64_t>(2 * P - 1 - src) * C + (startB - C);
+  const int64_t cntB = min64(lenB, max64(0, gq - gB0 + 1));
+  return static_cast<int>(cntA + cntB);
+}
+
+struct Unit {
+  int bh, g, rank, s_lo, s_hi, pair, part;
+  int64_t q_row0;  // first row of the rank's query chunk in the Q tensor
+};
+
+__device__ __forceinline__ Unit decode_unit(const AttnParams &p, int u) {
+  Unit w;
+  w.pair = u % p.n_pairs;
+  u /= p.n_pairs;
+  w.part = u % p.n_stepgroups;
+  u /= p.n_stepgroups;
+  const int ri = u % p.n_ranks;
+  u /= p.n_ranks;
+  w.g = u % p.G;
+  w.bh = u / p.G;
+  w.rank = p.rank_begin + ri;
+  w.s_lo = p.step_begin + w.part * p.steps_per_group;
+  w.s_hi = w.s_lo + p.steps_per_group;
+  w.q_row0 = static_cast<int64_t>(w.bh) * p.q_rows_bh + static_cast<int64_t>(w.g) * p.q_rows_g +
+             static_cast<int64_t>(ri) * p.L;
+  return w;
+}
+
+// Walks the key tiles of a unit in ring order: steps s_lo..s_hi-1, block
+// (rank - s) mod P, tiles of 128 keys; with the causal mask, tiles that no
+// query of the pair may see are skipped.
+struct TileIter {
+  int s, t;
+  int src;
+  __device__ __forceinline__ void settle(const AttnParams &p, const Unit &w, int n_t,
+                                         int64_t gq_max) {
+    while (s < w.s_hi) {
+      src = ((w.rank - s) % p.P + p.P) % p.P;
+      if (t >= n_t) {
+        t = 0;
+        ++s;
+        continue;
+      }
+      if (p.causal) {
+        const int64_t gk_min = zz_pos(src, static_cast<int64_t>(t) * kBN, p.L >> 1, p.P);
+        if (gk_min > gq_max) {
+          ++t;
+          continue;
+        }
+      }
+      return;
+    }
+  }
+  __device__ __forceinline__ bool valid(const Unit &w) const { return s < w.s_hi; }
+};
+
+template <int D, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    ring_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::kOffBar;
+  const uint32_t kv_full0 = bar0 + 8 * kBarKVFull;
+  const uint32_t kv_empty0 = kv_full0 + 8 * C::kSlots;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffBar + kAbortOff);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + kTmemSlotOff);
+  const Watchdog wd{p.wd.status, p.wd.limit_ns};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Unit w = decode_unit(p, blockIdx.x);
+  const int n_t = static_cast<int>((p.L + kBN - 1) / kBN);
+  const int64_t pair_row0 = static_cast<int64_t>(w.pair) * 2 * kBM;
+  const bool has_q1 = pair_row0 + kBM < p.L;
+  const int64_t half = p.L >> 1;
+  const int64_t gq_max =
+      p.causal ? zz_pos(w.rank, min64(pair_row0 + 2 * kBM - 1, p.L - 1), half, p.P) : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar0 + 8 * kBarQFull, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar0 + 8 * (kBarSFull + i), 1);
+      mbar_init(bar0 + 8 * (kBarPFull + i), 128);
+      mbar_init(bar0 + 8 * (kBarODone + i), 1);
+    }
+    mbar_init(bar0 + 8 * kBarDrain, 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(kv_full0 + 8 * s, 1);
+      mbar_init(kv_empty0 + 8 * s, 1);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      const uint32_t qfull = bar0 + 8 * kBarQFull;
+      const int32_t qy = static_cast<int32_t>(w.q_row0 + pair_row0);
+      mbar_arrive_expect_tx(qfull, 2 * C::kQTile);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_2d(sbase + C::kOffQ0 + c * C::kChunkBytes, &tm_q, c * 64, qy, qfull);
+        tma_load_2d(sbase + C::kOffQ1 + c * C::kChunkBytes, &tm_q, c * 64, qy + kBM, qfull);
+      }
+      const uint64_t keep = l2_policy_evict_last();
+      const int64_t kv_base =
+          static_cast<int64_t>(w.bh) * p.kv_rows_bh + static_cast<int64_t>(w.g) * p.kv_rows_g;
+      int it = 0;
+      TileIter ti{w.s_lo, 0, 0};
+      ti.settle(p, w, n_t, gq_max);
+      bool ok = true;
+      while (ok && ti.valid(w)) {
+        const int32_t ky = static_cast<int32_t>(kv_base + static_cast<int64_t>(ti.src) * p.L +
+                                                static_cast<int64_t>(ti.t) * kBN);
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const int slot = it % C::kSlots;
+          const uint32_t ph = (it / C::kSlots) & 1;
+          if (!mbar_wait(kv_empty0 + 8 * slot, ph ^ 1, wd, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(kv_full0 + 8 * slot, C::kKVTile);
+          const CUtensorMap *map = which ? &tm_v : &tm_k;
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_2d_hint(sbase + C::kOffKV + slot * C::kKVTile + c * C::kChunkBytes, map,
+                             c * 64, ky, kv_full0 + 8 * slot, keep);
+          ++it;
+        }
+        ++ti.t;
+        ti.settle(p, w, n_t, gq_max);
+      }
+      // Drain: every copy issued must land before the CTA may exit.
+      mbar_wait_drain(qfull, 0, p.wd.limit_ns);
+      for (int i = max(0, it - C::kSlots); i < it; ++i)
+        mbar_wait_drain(kv_full0 + 8 * (i % C::kSlots), (i / C::kSlots) & 1, p.wd.limit_ns);
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issue --
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
+      const uint32_t sQ[2] = {sbase + C::kOffQ0, sbase + C::kOffQ1};
+      const uint32_t sP[2] = {sbase + C::kOffP0, sbase + C::kOffP1};
+      const int nq = has_q1 ? 2 : 1;
+      bool issued = false;
+      TileIter ti{w.s_lo, 0, 0};
+      ti.settle(p, w, n_t, gq_max);
+      // S_i = Q_i K^T over d: K-major operands, 16 columns of d per MMA.
+      auto issue_s = [&](int i, int slot) {
+        const uint32_t kb = sbase + C::kOffKV + slot * C::kKVTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          mma_ss(tmem + col_s(i), smem_desc_sw128(sQ[i] + off, 16, 1024),
+                 smem_desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_i (+)= P_i V over 128 keys: P K-major, V MN-major (d contiguous).
+      auto issue_o = [&](int i, int slot, bool acc) {
+        const uint32_t vb = sbase + C::kOffKV + slot * C::kKVTile;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          mma_ss(tmem + col_o(i), smem_desc_sw128(sP[i] + aoff, 16, 1024),
+                 smem_desc_sw128(vb + kk * 2048, C::kChunkBytes, 1024), idesc_o,
+                 (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      if (ti.valid(w) && mbar_wait(bar0 + 8 * kBarQFull, 0, wd, abort_flag)) {
+        tc_fence_after();
+        int it = 0;  // slot sequence: K_j at 2j, V_j at 2j+1
+        bool ok = mbar_wait(kv_full0 + 8 * (it % C::kSlots), (it / C::kSlots) & 1, wd, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          for (int i = 0; i < nq; ++i) {
+            issue_s(i, it % C::kSlots);
+            mma_commit(bar0 + 8 * (kBarSFull + i));
+          }
+          mma_commit(kv_empty0 + 8 * (it % C::kSlots));
+          issued = true;
+          ++it;
+        }
+        for (int j = 0; ok; ++j) {
+          const int v_it = it;
+          ++ti.t;
+          ti.settle(p, w, n_t, gq_max);
+          const bool more = ti.valid(w);
+          if (!(ok = mbar_wait(kv_full0 + 8 * (v_it % C::kSlots), (v_it / C::kSlots) & 1, wd,
+                               abort_flag)))
+            break;
+          if (!(ok = mbar_wait(bar0 + 8 * kBarPFull, j & 1, wd, abort_flag))) break;
+          tc_fence_after();
+          issue_o(0, v_it % C::kSlots, j > 0);
+          const int k_it = v_it + 1;
+          if (more) {
+            if (!(ok = mbar_wait(kv_full0 + 8 * (k_it % C::kSlots), (k_it / C::kSlots) & 1, wd,
+                                 abort_flag)))
+              break;
+            tc_fence_after();
+            issue_s(0, k_it % C::kSlots);
+            mma_commit(bar0 + 8 * kBarSFull);
+          }
+          if (has_q1) {
+            if (!(ok = mbar_wait(bar0 + 8 * (kBarPFull + 1), j & 1, wd, abort_flag))) break;
+            tc_fence_after();
+            issue_o(1, v_it % C::kSlots, j > 0);
+          }
+          mma_commit(kv_empty0 + 8 * (v_it % C::kSlots));
+          if (!more) break;
+          if (has_q1) {
+            issue_s(1, k_it % C::kSlots);
+            mma_commit(bar0 + 8 * (kBarSFull + 1));
+          }
+          mma_commit(kv_empty0 + 8 * (k_it % C::kSlots));
+          it = k_it + 1;
+        }
+        if (ok) {
+          for (int i = 0; i < nq; ++i) mma_commit(bar0 + 8 * (kBarODone + i));
+        }
+      }
+      if (issued) {
+        // Nothing may still be running on the tensor core when TMEM is freed.
+        mma_commit(bar0 + 8 * kBarDrain);
+        mbar_wait_drain(bar0 + 8 * kBarDrain, 0, p.wd.limit_ns);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------- softmax --
+    const int wg = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    if (wg == 0 || has_q1) {
+      const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
+      const uint32_t tS = tmem + lane_bits + col_s(wg);
+      const uint32_t tO = tmem + lane_bits + col_o(wg);
+      const uint32_t sP = sbase + (wg ? C::kOffP1 : C::kOffP0);
+      const int64_t qi = pair_row0 + wg * kBM + row;  // row within the rank's chunk
+      const bool row_valid = qi < p.L;
+      const int64_t gq = p.causal ? zz_pos(w.rank, min64(qi, p.L - 1), half, p.P) : 0;
+      const float sl2 = p.scale_log2;
+      // Row-invariant part of this row's swizzled P address.
+      const uint32_t p_row = sP + (row >> 3) * 1024 + (row & 7) * 128;
+      const int sw = row & 7;
+
+      float m_ref = -INFINITY, l = 0.f;
+      int j = 0;
+      TileIter ti{w.s_lo, 0, 0};
+      ti.settle(p, w, n_t, gq_max);
+      while (ti.valid(w)) {
+        const bool ok =
+            __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarSFull + wg), j & 1, wd, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        float s[kBN];
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c)
+          tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(&s[c * 32]));
+        tmem_wait_ld();
+
+        const int64_t k0 = static_cast<int64_t>(ti.t) * kBN;
+        int nvis = static_cast<int>(min64(kBN, p.L - k0));
+        if (p.causal) nvis = causal_visible(ti.src, k0, gq, p.L, p.P);
+        if (nvis < kBN) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c >= nvis) s[c] = -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+        const float mxs = mx * sl2;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mxs > m_ref + kRescaleThreshold) {
+          if (m_ref != -INFINITY) {
+            alpha = ex2(m_ref - mxs);
+            rescale = true;
+          }
+          m_ref = mxs;
+        }
+        const float shift = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float rs = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < kBN / 8; ++cc) {
+          float e[8];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            e[x] = ex2(fmaf(s[cc * 8 + x], sl2, -shift));
+            rs += e[x];
+          }
+          const uint32_t addr = p_row + (cc >> 3) * C::kChunkBytes + (((cc & 7) ^ sw) << 4);
+          st_shared_v4(addr, pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
+                       pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+        }
+        l = l * alpha + rs;
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O holds the sum over earlier tiles (their PV finished before this
+          // tile's S was committed); scale it in place.
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] *= alpha;
+            tmem_st32(tO + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar0 + 8 * (kBarPFull + wg));
+        ++j;
+        ++ti.t;
+        ti.settle(p, w, n_t, gq_max);
+      }
+      __syncwarp();
+      const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
+      bool have_o = false;
+      if (j > 0 && !aborted) {
+        have_o = __all_sync(0xffffffffu,
+                            mbar_wait(bar0 + 8 * (kBarODone + wg), 0, wd, abort_flag));
+        tc_fence_after();
+      }
+      if (!aborted) {
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const float lse_val = (l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+        const int64_t orow = w.q_row0 + qi;
+        if (OUT_F32) {
+          float *out = reinterpret_cast<float *>(p.out) + w.part * p.out_part_stride + orow * D;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            if (have_o) {
+              tmem_ld32(tO + c * 32, o);
+              tmem_wait_ld();
+            } else {
+#pragma unroll
+              for (int x = 0; x < 32; ++x) o[x] = 0.f;
+            }
+            if (row_valid) {
+              float4 *dst = reinterpret_cast<float4 *>(out + c * 32);
+#pragma unroll
+              for (int x = 0; x < 8; ++x)
+                dst[x] = make_float4(o[4 * x] * inv_l, o[4 * x + 1] * inv_l, o[4 * x + 2] * inv_l,
+                                     o[4 * x + 3] * inv_l);
+            }
+          }
+        } else {
+          __nv_bfloat16 *out =
+              reinterpret_cast<__nv_bfloat16 *>(p.out) + w.part * p.out_part_stride + orow * D;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            if (have_o) {
+              tmem_ld32(tO + c * 32, o);
+              tmem_wait_ld();
+            } else {
+#pragma unroll
+              for (int x = 0; x < 32; ++x) o[x] = 0.f;
+            }
+            if (row_valid) {
+              uint4 *dst = reinterpret_cast<uint4 *>(out + c * 32);
+#pragma unroll
+              for (int x = 0; x < 4; ++x)
+                dst[x] = make_uint4(pack_bf16x2(o[8 * x] * inv_l, o[8 * x + 1] * inv_l),
+                                    pack_bf16x2(o[8 * x + 2] * inv_l, o[8 * x + 3] * inv_l),
+                                    pack_bf16x2(o[8 * x + 4] * inv_l, o[8 * x + 5] * inv_l),
+                                    pack_bf16x2(o[8 * x + 6] * inv_l, o[8 * x + 7] * inv_l));
+            }
+          }
+        }
+        if (row_valid) p.lse[w.part * p.lse_part_stride + orow] = lse_val;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// A kernel whose only wait can never complete (nothing arrives on the
+// barrier): exercises the bounded-wait path.
+__global__ void watchdog_selftest_kernel(WatchdogParams wdp) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const Watchdog wd{wdp.status, wdp.limit_ns};
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, wd, &abort_flag);
+  __syncthreads();
+}
+
+// --------------------------------------------------------------- host side --
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+// 2-D bf16 row matrix [rows, d], box = 128 rows x 64 elements (128 bytes),
+// 128-byte swizzle; rows past the end read as zero.
+cudaError_t make_row_map(CUtensorMap *map, const void *base, int64_t rows, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D, bool OUT_F32>
+cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                           const AttnParams &p, int64_t n_units, cudaStream_t stream) {
+  using C = Cfg<D>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(ring_attn_kernel<D, OUT_F32>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  ring_attn_kernel<D, OUT_F32><<<static_cast<unsigned>(n_units), kThreads, C::kSmemBytes, stream>>>(
+      mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k, const void *v,
+                             int64_t kv_total_rows, int d, bool out_f32, const AttnParams &p,
+                             cudaStream_t stream) {
+  const int64_t n_units = static_cast<int64_t>(p.BH) * p.G * p.n_ranks * p.n_stepgroups * p.n_pairs;
+  if (n_units <= 0) return cudaSuccess;
+  if (n_units > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  CUtensorMap mq, mk, mv;
+  cudaError_t e;
+  if ((e = make_row_map(&mq, q, q_total_rows, d)) != cudaSuccess) return e;
+  if ((e = make_row_map(&mk, k, kv_total_rows, d)) != cudaSuccess) return e;
+  if ((e = make_row_map(&mv, v, kv_total_rows, d)) != cudaSuccess) return e;
+  if (d == 128)
+    return out_f32 ? launch_variant<128, true>(mq, mk, mv, p, n_units, stream)
+                   : launch_variant<128, false>(mq, mk, mv, p, n_units, stream);
+  return out_f32 ? launch_variant<64, true>(mq, mk, mv, p, n_units, stream)
+                 : launch_variant<64, false>(mq, mk, mv, p, n_units, stream);
+}
+
+cudaError_t launch_watchdog_selftest(const WatchdogParams &wd, cudaStream_t stream) {
+  watchdog_selftest_kernel<<<1, 32, 0, stream>>>(wd);
+  return cudaGetLastError();
+}
+
+}  // namespace ra

@@ -1,0 +1,54 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ra {
+
+struct WatchdogParams {
+  int *status;       // device status word
+  int64_t limit_ns;  // bound on every barrier wait
+};
+
+// One launch of the blockwise ring-attention kernel.
+//
+// A "problem" is one (bh, g) pair: G independent attention problems per
+// (batch, head), e.g. the frames of spatial attention (G = 1 for the ring).
+// Each problem's keys form P ring blocks of L rows; a query chunk of rank r
+// (L rows) visits blocks (r - s) mod P for its steps s.  Work unit =
+// (bh, g, rank, step group, pair of 128-row query tiles); units are numbered
+// with the query-tile pair fastest, then step group, rank, g, bh.
+struct AttnParams {
+  int BH, G, n_ranks, n_stepgroups, n_pairs;
+  int64_t q_rows_bh, q_rows_g;    // Q / out / lse row strides (rows)
+  int64_t kv_rows_bh, kv_rows_g;  // K / V row strides (rows)
+  int64_t L;                      // rows per ring block (and per rank chunk)
+  int P, rank_begin, step_begin, steps_per_group;
+  int causal;                     // zigzag positions + key <= query mask
+  float scale_log2;               // log2(e) / sqrt(d)
+  void *out;                      // bf16 or fp32
+  float *lse;
+  int64_t out_part_stride;        // elements between step groups' outputs
+  int64_t lse_part_stride;
+  WatchdogParams wd;
+};
+
+// Launches the attention kernel.  q/k/v: bf16 row matrices [rows, d].
+cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k, const void *v,
+                             int64_t kv_total_rows, int d, bool out_f32, const AttnParams &p,
+                             cudaStream_t stream);
+
+// Row permutation kernels (shard.cu).  mode: 0 shard, 1 unshard (layout, P),
+// 2 frame transpose [T,N] -> [N,T], 3 back.  row_bytes: 128, 256 (bf16 rows) or 4 (fp32).
+cudaError_t launch_row_permute(const void *x, void *y, int64_t BH, int64_t S, int row_bytes,
+                               int mode, int64_t a, int64_t b, int layout, cudaStream_t stream);
+
+// lse_merge kernel (merge.cu).
+cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int n, int64_t rows,
+                             int d, void *out, float *lse_out, cudaStream_t stream);
+
+// Watchdog self-test kernel (attn_fwd.cu).
+cudaError_t launch_watchdog_selftest(const WatchdogParams &wd, cudaStream_t stream);
+
+}  // namespace ra

@@ -1,0 +1,124 @@
+// Row permutations of [BH, S, row] tensors: sequence sharding for context
+// parallelism and the frame transpose of factored video attention.
+//
+// Sharding ("day 83" blog, "Context parallelism: splitting the sequence";
+// k8ai "How context parallel works", balanced causal split read as zigzag):
+// sharded row j = r*L + i of rank r holds global token
+//   contiguous: r*L + i
+//   zigzag:     r*C + i (i < C), (2P-1-r)*C + (i - C) (i >= C),  C = S/(2P).
+// Frame transpose ("day 83" blog, "The spatial-temporal twist"): token t*N + n
+// of [T, N] order is row n*T + t of [N, T] order.
+//
+// Each thread moves 16-byte pieces (or 4-byte elements for fp32 rows) with
+// plain vector loads/stores; consecutive threads take consecutive pieces of a
+// row, so both sides are fully coalesced 128-byte lines.
+#include <stdint.h>
+
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+struct PermuteArgs {
+  int64_t S;
+  int mode;       // 0 shard, 1 unshard, 2 [T,N]->[N,T], 3 [N,T]->[T,N]
+  int64_t a, b;   // modes 0/1: a = P; modes 2/3: a = T, b = N
+  int layout;     // modes 0/1: 0 contiguous, 1 zigzag
+};
+
+// Source row (within one (b,h) slice) of output row o.
+__device__ __forceinline__ int64_t source_row(const PermuteArgs &p, int64_t o) {
+  switch (p.mode) {
+    case 0: {  // y[j] = x[s2g(j)]
+      if (p.layout == 0) return o;
+      const int64_t P = p.a, L = p.S / P, C = L >> 1;
+      const int64_t r = o / L, i = o - r * L;
+      return i < C ? r * C + i : (2 * P - 1 - r) * C + (i - C);
+    }
+    case 1: {  // y[g] = x[g2s(g)]
+      if (p.layout == 0) return o;
+      const int64_t P = p.a, L = p.S / P, C = L >> 1;
+      const int64_t chunk = o / C, off = o - chunk * C;
+      return chunk < P ? chunk * L + off : (2 * P - 1 - chunk) * L + C + off;
+    }
+    case 2: {  // output [N, T]: row n*T + t <- input row t*N + n
+      const int64_t T = p.a, N = p.b;
+      const int64_t n = o / T, t = o - n * T;
+      return t * N + n;
+    }
+    default: {  // output [T, N]: row t*N + n <- input row n*T + t
+      const int64_t T = p.a, N = p.b;
+      const int64_t t = o / N, n = o - t * N;
+      return n * T + t;
+    }
+  }
+}
+
+template <typename Vec, int PIECES>
+__global__ void __launch_bounds__(256) row_permute_kernel(const Vec *__restrict__ x,
+                                                          Vec *__restrict__ y, int64_t total_rows,
+                                                          PermuteArgs p) {
+  constexpr int kUnroll = 4;
+  const int64_t total = total_rows * PIECES;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; idx < total; idx += kUnroll * stride) {
+    Vec v[kUnroll];
+    int64_t dst[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t e = idx + u * stride;
+      dst[u] = -1;
+      if (e < total) {
+        const int64_t row = e / PIECES;
+        const int piece = static_cast<int>(e - row * PIECES);
+        const int64_t bh = row / p.S, o = row - bh * p.S;
+        const int64_t src = bh * p.S + source_row(p, o);
+        v[u] = x[src * PIECES + piece];
+        dst[u] = e;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (dst[u] >= 0) y[dst[u]] = v[u];
+  }
+}
+
+int grid_for(int64_t work, int threads) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (work + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 resident 256-thread blocks per SM
+  return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_row_permute(const void *x, void *y, int64_t BH, int64_t S, int row_bytes,
+                               int mode, int64_t a, int64_t b, int layout, cudaStream_t stream) {
+  const int64_t rows = BH * S;
+  if (rows == 0) return cudaSuccess;
+  PermuteArgs p{S, mode, a, b, layout};
+  if (row_bytes % 16 == 0) {
+    const int pieces = row_bytes / 16;
+    const int grid = grid_for(rows * pieces / 4, 256);
+    if (pieces == 16)
+      row_permute_kernel<uint4, 16><<<grid, 256, 0, stream>>>(
+          static_cast<const uint4 *>(x), static_cast<uint4 *>(y), rows, p);
+    else if (pieces == 8)
+      row_permute_kernel<uint4, 8><<<grid, 256, 0, stream>>>(
+          static_cast<const uint4 *>(x), static_cast<uint4 *>(y), rows, p);
+    else
+      return cudaErrorInvalidValue;
+  } else if (row_bytes == 4) {
+    const int grid = grid_for(rows / 4, 256);
+    row_permute_kernel<uint32_t, 1><<<grid, 256, 0, stream>>>(
+        static_cast<const uint32_t *>(x), static_cast<uint32_t *>(y), rows, p);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ra

@@ -101,16 +101,17 @@ def make_custom(shape_q, shape_kv, seed, factor=1.0):
     return q, k, v
 
 
-def make_partials(n, rows, d, seed, empty_rows=0, empty_parts=0):
+def make_partials(n, rows, d, seed, empty_rows=0, empty_parts=0, o_scale=0.25):
     """Seeded fp32 partial outputs and log-sum-exps for merge tests.
 
     Returns o [n, rows, d] fp32 and lse [n, rows] fp32.  The first `empty_rows`
     rows have every partial empty (lse = -inf, o = 0); in the next rows, the
-    first `empty_parts` partials are empty.  Everything else is N(0,1) for o and
-    N(0, 2^2) for lse.
+    first `empty_parts` partials are empty.  Everything else is N(0, o_scale^2)
+    for o (a normalised attention output is a convex combination of value rows,
+    so its entries are small) and N(0, 2^2) for lse.
     """
     g = torch.Generator("cpu").manual_seed(seed)
-    o = torch.randn((n, rows, d), generator=g, dtype=torch.float32)
+    o = torch.randn((n, rows, d), generator=g, dtype=torch.float32) * o_scale
     lse = torch.randn((n, rows), generator=g, dtype=torch.float32) * 2.0
     if empty_rows:
         o[:, :empty_rows] = 0.0

@@ -1,0 +1,267 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances: max |O_gpu - O_ref| <= 1e-2 and max |LSE_gpu - LSE_ref| <= 1e-3
+(bf16 inputs, fp32 accumulation, bf16 output); index maps and permutations
+bit-exact.  Outputs are un-sharded with the oracle's own index map before
+comparison, so the check does not rely on the CUDA permutation.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import ring_attention_attn_gb300 as ra
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+def _shard_host(x, P, layout):
+    """Global -> sharded order using the oracle's map (CPU)."""
+    s2g, _ = oracle.shard_index(x.shape[2], P, layout)
+    return x[:, :, torch.from_numpy(s2g)].contiguous()
+
+
+def _unshard_host(y, P, layout):
+    _, g2s = oracle.shard_index(y.shape[2], P, layout)
+    return y[:, :, torch.from_numpy(g2s)].contiguous()
+
+
+def _cmp(o_gpu, lse_gpu, o_ref, lse_ref, o_tol=O_TOL, lse_tol=LSE_TOL):
+    o_gpu = o_gpu.double().cpu().numpy().reshape(o_ref.shape)
+    lse_gpu = lse_gpu.double().cpu().numpy().reshape(lse_ref.shape)
+    eo = np.max(np.abs(o_gpu - o_ref)) if o_ref.size else 0.0
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(fin, np.isfinite(lse_gpu)), "-inf pattern of LSE differs"
+    el = np.max(np.abs(lse_gpu[fin] - lse_ref[fin])) if fin.any() else 0.0
+    assert eo <= o_tol, f"max|dO| = {eo:.3e}"
+    assert el <= lse_tol, f"max|dLSE| = {el:.3e}"
+    return eo, el
+
+
+def _run_ring(q, k, v, P, causal):
+    layout = 1 if causal else 0
+    qs, ks, vs = (_shard_host(x, P, layout).cuda() for x in (q, k, v))
+    out, lse = ra.ring_attn_fwd(qs, ks, vs, P, causal=causal)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+    return (_unshard_host(out.cpu(), P, layout),
+            _unshard_host(lse.cpu().unsqueeze(-1), P, layout).squeeze(-1))
+
+
+# ----------------------------------------------------------- permutations --
+@pytest.mark.parametrize("S,P,layout,d", [(4096, 2, 1, 64), (1024, 4, 0, 64), (48, 4, 1, 128),
+                                          (14400, 4, 0, 128), (600, 3, 1, 128), (16, 8, 1, 64)])
+def test_cp_shard_bit_exact(S, P, layout, d):
+    x, _, _ = synth.make_custom((2, 3, S, d), (1, 1, 1, d), seed=S + P)
+    y = ra.ra_cp_shard(x.cuda(), P, layout)
+    assert torch.equal(y.cpu().view(torch.int16), _shard_host(x, P, layout).view(torch.int16))
+    back = ra.ra_cp_shard(y, P, layout, inverse=True)
+    assert torch.equal(back.cpu().view(torch.int16), x.view(torch.int16))
+
+
+def test_cp_shard_index_matches_oracle():
+    for S, P, layout in [(4096, 2, 1), (1024, 4, 0), (600, 3, 1), (432000, 8, 0), (64, 8, 1)]:
+        a = ra.ra_cp_shard_index(S, P, layout)
+        b = oracle.shard_index(S, P, layout)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("T,N,d", [(48, 900, 128), (5, 7, 64)])
+def test_frame_transpose_bit_exact(T, N, d):
+    x, _, _ = synth.make_custom((1, 3, T * N, d), (1, 1, 1, d), seed=T * N)
+    y = ra.ra_frame_transpose(x.cuda(), T, N)
+    ref = x.reshape(1, 3, T, N, d).transpose(2, 3).reshape(1, 3, T * N, d)
+    assert torch.equal(y.cpu().view(torch.int16), ref.view(torch.int16))
+    back = ra.ra_frame_transpose(y, T, N, inverse=True)
+    assert torch.equal(back.cpu().view(torch.int16), x.view(torch.int16))
+
+
+# ------------------------------------------------------------------ merge --
+@pytest.mark.parametrize("n,rows,d,empty_rows,empty_parts",
+                         [(8, 1000, 128, 3, 2), (3, 777, 64, 1, 1), (1, 50, 128, 0, 0),
+                          (17, 300, 64, 5, 9)])
+def test_lse_merge(n, rows, d, empty_rows, empty_parts):
+    o, l = synth.make_partials(n, rows, d, seed=n * rows, empty_rows=empty_rows,
+                               empty_parts=empty_parts)
+    om, lm = ra.lse_merge(o.cuda(), l.cuda())
+    ro, rl = oracle.lse_merge(o.double().numpy(), l.double().numpy())
+    _cmp(om, lm, ro, rl)
+    assert torch.all(om[:empty_rows].float() == 0)
+
+
+# -------------------------------------------------------------- attention --
+def test_ring_c1_full():
+    w = synth.WORKLOADS["c1"]
+    q, k, v = synth.make_qkv(w)
+    o, l = _run_ring(q, k, v, w.P, w.causal)
+    ro, rl = oracle.attention(q, k, v, causal=False)
+    _cmp(o, l, ro, rl)
+
+
+def test_ring_c2_causal_zigzag_full():
+    w = synth.WORKLOADS["c2"]
+    q, k, v = synth.make_qkv(w)
+    o, l = _run_ring(q, k, v, w.P, w.causal)
+    ro, rl = oracle.attention(q, k, v, causal=True)
+    _cmp(o, l, ro, rl)
+
+
+CASES = [
+    # B, H, S, d, P, causal  -- ragged tails, tiny chunks, P = 1, C not a tile multiple
+    (1, 2, 1000, 64, 4, False),
+    (2, 1, 520, 128, 2, False),
+    (1, 1, 8, 64, 2, False),
+    (1, 2, 300, 128, 1, False),
+    (1, 1, 1, 128, 1, False),
+    (1, 2, 600, 128, 3, True),
+    (1, 1, 1024, 128, 4, True),
+    (2, 2, 520, 64, 2, True),
+    (1, 1, 16, 64, 8, True),
+    (1, 3, 2048, 128, 8, False),
+]
+
+
+@pytest.mark.parametrize("B,H,S,d,P,causal", CASES)
+def test_ring_small_cases(B, H, S, d, P, causal):
+    q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=S * 7 + d + P)
+    o, l = _run_ring(q, k, v, P, causal)
+    ro, rl = oracle.attention(q, k, v, causal=causal)
+    _cmp(o, l, ro, rl)
+
+
+def test_ring_c3_sampled_rows():
+    w = synth.WORKLOADS["c3"]
+    q, k, v = synth.make_qkv(w)
+    o, l = _run_ring(q, k, v, w.P, w.causal)
+    per = synth.sample_rows(w, 48)
+    rows = oracle.flat_rows(w.B, w.H, w.S, per)
+    ro, rl = oracle.attention(q, k, v, rows=rows)
+    _cmp(o.reshape(-1, w.d)[rows], l.reshape(-1)[rows], ro, rl)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rank_partials_and_merge(causal):
+    B, H, S, d, P, rank = 1, 2, 4096, 128, 8, 3
+    layout = 1 if causal else 0
+    q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=55 + causal)
+    qs, ks, vs = (_shard_host(x, P, layout) for x in (q, k, v))
+    L = S // P
+    q_local = qs[:, :, rank * L:(rank + 1) * L].contiguous().cuda()
+    kd, vd = ks.cuda(), vs.cuda()
+    parts, lparts = ra.ring_attn_fwd_rank(q_local, kd, vd, P, rank, causal=causal, out_fp32=True)
+    fused, lfused = ra.ring_attn_fwd_rank(q_local, kd, vd, P, rank, causal=causal)
+    merged, lmerged = ra.lse_merge(parts, lparts)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+    s2g, _ = oracle.shard_index(S, P, layout)
+    gq = s2g[rank * L:(rank + 1) * L]
+    # every per-step partial against the oracle on that block's keys
+    for s in range(P):
+        src = oracle.ring_source(P, rank, s)
+        blk = torch.from_numpy(s2g[src * L:(src + 1) * L])
+        kb, vb = k[:, :, blk], v[:, :, blk]
+        ro = np.empty((B, H, L, d))
+        rl = np.empty((B, H, L))
+        qg = q[:, :, torch.from_numpy(gq)]
+        if causal:
+            # keys of this block visible to each query: global key <= global query
+            for i in range(L):
+                vis = torch.from_numpy(np.nonzero(s2g[src * L:(src + 1) * L] <= gq[i])[0])
+                oi, li = oracle.attention(qg[:, :, i:i + 1], kb[:, :, vis], vb[:, :, vis])
+                ro[:, :, i], rl[:, :, i] = oi[:, :, 0], li[:, :, 0]
+        else:
+            ro, rl = oracle.attention(qg, kb, vb)
+        _cmp(parts[s], lparts[s], ro, rl)
+    ro, rl = oracle.attention(q, k, v, causal=causal, rows=oracle.flat_rows(B, H, S, gq))
+    _cmp(merged, lmerged, ro, rl)
+    _cmp(fused, lfused, ro, rl)
+    assert (merged.float() - fused.float()).abs().max().item() <= 4e-3
+
+
+def test_rank_step_subrange():
+    B, H, S, d, P, rank = 1, 1, 2048, 64, 4, 2
+    q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=77)
+    L = S // P
+    qd, kd, vd = q[:, :, rank * L:(rank + 1) * L].contiguous().cuda(), k.cuda(), v.cuda()
+    o, l = ra.ring_attn_fwd_rank(qd, kd, vd, P, rank, step_begin=1, step_end=3)
+    blocks = [oracle.ring_source(P, rank, s) for s in (1, 2)]
+    idx = torch.cat([torch.arange(b * L, (b + 1) * L) for b in blocks])
+    ro, rl = oracle.attention(q[:, :, rank * L:(rank + 1) * L], k[:, :, idx], v[:, :, idx])
+    _cmp(o, l, ro, rl)
+
+
+def test_c5_full_size_sampled():
+    """One rank's 54,000 queries against 432,000 keys: per-step partials +
+    lse_merge (the benchmark's launch configuration) and the fused call."""
+    w = synth.WORKLOADS["c5"]
+    q, k, v = synth.make_qkv(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    parts, lparts = ra.ring_attn_fwd_rank(qd, kd, vd, w.P, 0, out_fp32=True)
+    o, l = ra.lse_merge(parts, lparts)
+    fo, fl = ra.ring_attn_fwd_rank(qd, kd, vd, w.P, 0)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+    per = synth.sample_rows(w, 12)
+    rows = oracle.flat_rows(w.B, w.H, w.L, per)
+    ro, rl = oracle.attention(q, k, v, rows=rows)
+    _cmp(o.reshape(-1, w.d)[rows.tolist()], l.reshape(-1)[rows.tolist()], ro, rl)
+    _cmp(fo.reshape(-1, w.d)[rows.tolist()], fl.reshape(-1)[rows.tolist()], ro, rl)
+    assert (o.float() - fo.float()).abs().max().item() <= 2e-3
+
+
+# ---------------------------------------------------------------- factored --
+def test_factored_small_full():
+    B, H, T, N, d, P = 1, 2, 8, 50, 64, 4
+    q, k, v = synth.make_custom((B, H, T * N, d), (B, H, T * N, d), seed=99)
+    os_, ls, ot, lt = ra.factored_attn(q.cuda(), k.cuda(), v.cuda(), T, N, P)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+    ro, rl = oracle.factored(q, k, v, T, N, "spatial")
+    _cmp(os_, ls, ro, rl)
+    ro, rl = oracle.factored(q, k, v, T, N, "temporal")
+    _cmp(ot, lt, ro, rl)
+
+
+def test_factored_c4_sampled():
+    w = synth.WORKLOADS["c4"]
+    q, k, v = synth.make_qkv(w)
+    os_, ls, ot, lt = ra.factored_attn(q.cuda(), k.cuda(), v.cuda(), w.T, w.N, w.P)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+    rng = np.random.default_rng(1003)
+    per = np.unique(np.concatenate([[0, w.S - 1, w.N - 1, w.N], rng.integers(0, w.S, 60)]))
+    rows = oracle.flat_rows(w.B, w.H, w.S, per)
+    ro, rl = oracle.factored(q, k, v, w.T, w.N, "spatial", rows=rows)
+    _cmp(os_.reshape(-1, w.d)[rows.tolist()], ls.reshape(-1)[rows.tolist()], ro, rl)
+    ro, rl = oracle.factored(q, k, v, w.T, w.N, "temporal", rows=rows)
+    _cmp(ot.reshape(-1, w.d)[rows.tolist()], lt.reshape(-1)[rows.tolist()], ro, rl)
+
+
+# ---------------------------------------------------------- edge + status --
+def test_empty_inputs_are_noops():
+    z = torch.empty((1, 0, 64, 64), dtype=torch.bfloat16, device="cuda")
+    out, lse = ra.ring_attn_fwd(z, z, z, 2)
+    z2 = torch.empty((1, 1, 0, 64), dtype=torch.bfloat16, device="cuda")
+    ra.ring_attn_fwd(z2, z2, z2, 2)
+    assert ra.ra_get_status() == 0
+
+
+def test_watchdog_reports_timeout():
+    ra.ra_set_watchdog_ns(1_000_000)  # 1 ms
+    try:
+        ra.ra_watchdog_selftest()
+        assert ra.ra_get_status() == -5
+        assert ra.ra_get_status() == 0  # cleared by the read
+    finally:
+        ra.ra_set_watchdog_ns(0)
+    # the context is still usable afterwards
+    q, k, v = synth.make_custom((1, 1, 256, 64), (1, 1, 256, 64), seed=3)
+    o, l = _run_ring(q, k, v, 2, False)
+    ro, rl = oracle.attention(q, k, v)
+    _cmp(o, l, ro, rl)
