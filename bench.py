@@ -43,6 +43,9 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--kv-len", type=int, default=0,
+                    help="smaller total sequence (same kernels and launch shape) for profiling")
+    ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
 
 
@@ -131,6 +134,16 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def _workload(a):
+    import dataclasses
+    import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    if a.kv_len:
+        assert a.kv_len % (w.P * 2) == 0
+        w = dataclasses.replace(w, S=a.kv_len)
+    return w
+
+
 def _cpu_baseline(seconds_target, quick_rows=4):
     """Time the fp64 oracle on sampled c5 query rows (host cores)."""
     import numpy as np
@@ -210,7 +223,7 @@ def run_ours(a, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
-    w = synth.WORKLOADS[WORKLOAD]
+    w = _workload(a)
     q, k, v = synth.make_qkv(w)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     n = w.P
@@ -289,7 +302,10 @@ def run_ours(a, rank, world, local):
         oh.copy_(out, non_blocking=True)
         lh.copy_(lse, non_blocking=True)
 
-    e2e_step()
+    if a.no_e2e:
+        e2e_steps = 0
+    else:
+        e2e_step()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -300,12 +316,12 @@ def run_ours(a, rank, world, local):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = e0.elapsed_time(e1) if e2e_steps else float("nan")
     if dist is not None:
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
-    e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_value = (world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12) if e2e_steps else None
     h2d = (q.numel() + k.numel() + v.numel()) * 2
     d2h = out.numel() * 2 + lse.numel() * 4
 
@@ -319,7 +335,9 @@ def run_ours(a, rank, world, local):
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": total_ms / a.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "B": w.B, "H": w.H, "S": w.S, "d": w.d,
+            "config": {"workload": WORKLOAD_DESC if not a.kv_len else
+                       f"reduced profiling case of the same path: S={w.S}",
+                       "B": w.B, "H": w.H, "S": w.S, "d": w.d,
                        "P": w.P, "rank": 0, "seq_len": w.S, "global_batch": w.B,
                        "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (K+V 884.7 MB per replica)"},
@@ -338,7 +356,7 @@ def run_ours(a, rank, world, local):
             "clocks": clock_info,
             "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "ms_per_step": e2e_ms / e2e_steps},
+                    "ms_per_step": (e2e_ms / e2e_steps) if e2e_steps else None},
             "gpu_launches": 2 * a.steps,
         }
         if cpu is not None:

@@ -14,7 +14,8 @@ import threading
 import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libringattn.so")
+# RINGATTN_LIB selects another build of the same library (same ABI).
+LIB_PATH = os.environ.get("RINGATTN_LIB") or os.path.join(HERE, "libringattn.so")
 
 RA_OK = 0
 ERRORS = {-1: "RA_ERR_ARG", -2: "RA_ERR_SHAPE", -3: "RA_ERR_ALIGN", -4: "RA_ERR_CUDA",
