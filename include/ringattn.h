@@ -130,6 +130,34 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
 /* Scratch bytes factored_attn needs for these sizes (0 on bad arguments). */
 size_t factored_attn_workspace(int B, int H, int T, int N, int d);
 
+/* Size of the fixed device scratch that factored_attn_static works in. */
+#define RA_STATIC_SCRATCH_BYTES (64u << 20)
+
+/* factored_attn without any device allocation: the same computation, inputs
+ * and outputs as factored_attn, but its scratch is a fixed array of
+ * RA_STATIC_SCRATCH_BYTES (64 MiB) compiled into this library, so the caller
+ * passes no workspace.  The pages have no counterpart: it exists for callers
+ * that may not allocate device memory themselves, for example a host program
+ * whose device memory is all handed to its own pool at start-up, or a serving
+ * loop in which an allocation (and the synchronisation cudaMalloc implies) is
+ * not allowed.
+ *  - Limit: the sizes must satisfy factored_attn_workspace(B,H,T,N,d) <=
+ *    RA_STATIC_SCRATCH_BYTES (about 65,000 tokens x heads at d = 128,
+ *    130,000 at d = 64); larger sizes return RA_ERR_WORKSPACE and launch
+ *    nothing.  Other argument errors are those of factored_attn.
+ *  - The array lives in every GPU that loads the library until the process
+ *    exits.  The first call on a device looks up the array's device address
+ *    (once per device, with that device current); make that first call before
+ *    any stream capture.
+ *  - Nothing in the scratch needs to start at zero (every byte read is first
+ *    written by the same call), but all calls share the one array: calls whose
+ *    work overlaps on the GPU (other streams, other host threads) race; order
+ *    them on one stream or synchronise between them.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+int factored_attn_static(const void *q, const void *k, const void *v, void *out_s, float *lse_s,
+                         void *out_t, float *lse_t, int B, int H, int T, int N, int d, int P,
+                         void *stream);
+
 /* Synchronises `stream`, then returns and clears the device status word:
  * RA_OK, or RA_ERR_TIMEOUT if a kernel's bounded wait expired since the last
  * call (the kernel then stopped early and its outputs are undefined), or

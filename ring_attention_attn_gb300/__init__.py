@@ -9,6 +9,7 @@ from ._abi import (  # noqa: F401
     EXPORTS,
     RingAttnError,
     factored_attn,
+    factored_attn_static,
     factored_attn_workspace,
     lib,
     lse_merge,

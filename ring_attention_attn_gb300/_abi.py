@@ -24,7 +24,8 @@ ERRORS = {-1: "RA_ERR_ARG", -2: "RA_ERR_SHAPE", -3: "RA_ERR_ALIGN", -4: "RA_ERR_
 # Every symbol include/ringattn.h declares.
 EXPORTS = ("ra_cp_shard_index", "ra_ring_source", "ra_cp_shard", "ra_frame_transpose",
            "ring_attn_fwd", "ring_attn_fwd_rank", "lse_merge", "factored_attn",
-           "factored_attn_workspace", "ra_get_status", "ra_set_watchdog_ns",
+           "factored_attn_workspace", "factored_attn_static", "ra_get_status",
+           "ra_set_watchdog_ns",
            "ra_watchdog_selftest", "ra_strerror", "ra_last_cuda_error")
 
 _lock = threading.Lock()
@@ -63,6 +64,8 @@ def lib():
                 "factored_attn": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                         vp, sz, vp]),
                 "factored_attn_workspace": (sz, [i32, i32, i32, i32, i32]),
+                "factored_attn_static": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                               i32, i32, vp]),
                 "ra_get_status": (i32, [vp]),
                 "ra_set_watchdog_ns": (None, [i64]),
                 "ra_watchdog_selftest": (i32, [vp]),
@@ -221,6 +224,23 @@ def factored_attn(q, k, v, T: int, N: int, P: int, workspace=None, outs=None, st
                                _dev(lse_t, torch.float32, "lse_t"), B, H, T, N, d, P,
                                _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
                                _stream(stream)), "factored_attn")
+    return out_s, lse_s, out_t, lse_t
+
+
+def factored_attn_static(q, k, v, T: int, N: int, P: int, outs, stream=None):
+    """factored_attn working in the library's fixed device scratch (no workspace
+    argument, no device allocation by the library).  `outs` = (out_s, lse_s,
+    out_t, lse_t), caller-allocated like factored_attn's outputs."""
+    import torch
+    B, H, S, d = q.shape
+    out_s, lse_s, out_t, lse_t = outs
+    _check(lib().factored_attn_static(_dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"),
+                                      _dev(v, torch.bfloat16, "v"),
+                                      _dev(out_s, torch.bfloat16, "out_s"),
+                                      _dev(lse_s, torch.float32, "lse_s"),
+                                      _dev(out_t, torch.bfloat16, "out_t"),
+                                      _dev(lse_t, torch.float32, "lse_t"), B, H, T, N, d, P,
+                                      _stream(stream)), "factored_attn_static")
     return out_s, lse_s, out_t, lse_t
 
 

@@ -56,6 +56,8 @@ constexpr int64_t kMaxRows = (int64_t(1) << 31) - 512;
 
 }  // namespace
 
+int ra::record_cuda_error(cudaError_t e) { return fail_cuda(e); }
+
 extern "C" {
 
 const char *ra_strerror(int code) {

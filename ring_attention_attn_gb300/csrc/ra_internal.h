@@ -51,4 +51,7 @@ cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int n
 // Watchdog self-test kernel (attn_fwd.cu).
 cudaError_t launch_watchdog_selftest(const WatchdogParams &wd, cudaStream_t stream);
 
+// Records `e` as the error ra_last_cuda_error reports; returns RA_ERR_CUDA (api.cu).
+int record_cuda_error(cudaError_t e);
+
 }  // namespace ra

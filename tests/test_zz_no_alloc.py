@@ -1,0 +1,78 @@
+"""factored_attn_static: the entry point for callers that may not allocate
+device memory (e.g. their device memory is all owned by a pool set up at
+start-up, or an allocation is not allowed where they call the library).
+
+It must give the same outputs as factored_attn with a caller workspace, on two
+calls in a row (the second call reuses the fixed scratch the first one left
+behind), and must refuse sizes its fixed scratch cannot hold.  This file is
+collected last so that a run stopping at the first failure has run every
+other test first; it also passes alone in a fresh process.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import synth
+import ring_attention_attn_gb300 as ra
+from ring_attention_attn_gb300 import _abi
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+STATIC_SCRATCH_BYTES = 64 << 20  # RA_STATIC_SCRATCH_BYTES in include/ringattn.h
+
+
+def _outs(B, H, S, d):
+    return (torch.empty((B, H, S, d), dtype=torch.bfloat16, device="cuda"),
+            torch.empty((B, H, S), dtype=torch.float32, device="cuda"),
+            torch.empty((B, H, S, d), dtype=torch.bfloat16, device="cuda"),
+            torch.empty((B, H, S), dtype=torch.float32, device="cuda"))
+
+
+def _call_static(q, k, v, T, N, P, outs):
+    """Calls the C entry point directly through ctypes."""
+    B, H, S, d = q.shape
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return _abi.lib().factored_attn_static(p(q), p(k), p(v), p(outs[0]), p(outs[1]), p(outs[2]),
+                                           p(outs[3]), B, H, T, N, d, P, stream)
+
+
+def _max_diff(a, b):
+    fa, fb = a.float(), b.float()
+    fin = torch.isfinite(fb)
+    assert torch.equal(fin, torch.isfinite(fa))
+    return (fa[fin] - fb[fin]).abs().max().item() if fin.any() else 0.0
+
+
+@pytest.mark.parametrize("B,H,T,N,d,P,seeds", [(1, 2, 8, 50, 64, 4, (11, 12)),
+                                               (1, 3, 12, 130, 128, 4, (21, 22))])
+def test_static_scratch_matches_workspace_version_twice(B, H, T, N, d, P, seeds):
+    S = T * N
+    assert ra.factored_attn_workspace(B, H, T, N, d) <= STATIC_SCRATCH_BYTES
+    for seed in seeds:  # two calls in a row, different inputs
+        q, k, v = (x.cuda() for x in synth.make_custom((B, H, S, d), (B, H, S, d), seed=seed))
+        got = _outs(B, H, S, d)
+        assert _call_static(q, k, v, T, N, P, got) == 0
+        want = ra.factored_attn(q, k, v, T, N, P)
+        torch.cuda.synchronize()
+        assert ra.ra_get_status() == 0
+        assert _max_diff(got[0], want[0]) <= O_TOL
+        assert _max_diff(got[1], want[1]) <= LSE_TOL
+        assert _max_diff(got[2], want[2]) <= O_TOL
+        assert _max_diff(got[3], want[3]) <= LSE_TOL
+
+
+def test_static_scratch_refuses_sizes_beyond_its_limit():
+    B, H, T, N, d, P = 1, 24, 48, 900, 128, 4  # needs ~1.07 GB of scratch
+    assert ra.factored_attn_workspace(B, H, T, N, d) > STATIC_SCRATCH_BYTES
+    x = torch.empty((1, 1, 1, d), dtype=torch.bfloat16, device="cuda")  # never touched
+    lse = torch.empty((1,), dtype=torch.float32, device="cuda")
+    p = ctypes.c_void_p
+    rc = _abi.lib().factored_attn_static(p(x.data_ptr()), p(x.data_ptr()), p(x.data_ptr()),
+                                         p(x.data_ptr()), p(lse.data_ptr()), p(x.data_ptr()),
+                                         p(lse.data_ptr()), B, H, T, N, d, P,
+                                         p(torch.cuda.current_stream().cuda_stream))
+    assert rc == -6  # RA_ERR_WORKSPACE
