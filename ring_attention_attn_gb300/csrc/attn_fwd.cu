@@ -11,18 +11,23 @@
 // and finally writes O / l and LSE = m + ln l.  Scores are q.k / sqrt(d),
 // masked by global token position (key <= query) for the zigzag causal split.
 //
-// CTA structure (384 threads, one CTA per SM, 230 KB shared memory):
+// CTA structure (384 threads, one CTA per SM, ~225 KB shared memory):
 //   warp 0       TMA producer: Q tile pair once, then K_j, V_j tiles through a
 //                ring of shared-memory slots (mbarrier full/empty pairs).
 //   warp 1       allocates 512 TMEM columns; one thread issues every
 //                tcgen05.mma and tcgen05.commit.
 //   warps 4..7   softmax for query tile 0 (one thread per query row),
 //   warps 8..11  softmax for query tile 1; the two tiles ping-pong so the
-//                tensor core computes one tile's QK^T / PV while the other
-//                tile's softmax runs.
+//                tensor core computes one tile's PV / next QK^T while the
+//                other tile's softmax runs.
+//   The producer/MMA warpgroup hands registers to the softmax warpgroups
+//   (setmaxnreg).
 // Tensor memory: S0 cols [0,128), S1 [128,256), O0 [256,256+d), O1 [384,384+d).
-// P (bf16 probabilities) goes through shared memory in the 128-byte-swizzled
-// K-major layout the MMA reads, so both MMAs take their operands from SMEM.
+// P (bf16 probabilities) overwrites the first 64 columns of its tile's S (one
+// bf16 pair per 32-bit column) and is the A operand of the PV MMA straight
+// from tensor memory; QK^T takes both operands from shared memory.  Because
+// P_i lives in S_i's columns, S_i of the next tile is issued after PV_i of
+// this one; the MMAs of one thread execute in issue order.
 //
 // The O rescale is lazy: a row's reference max only moves when the new max
 // exceeds it by more than 2^8 (in exp2 units), so P entries stay <= 256 and
@@ -47,15 +52,13 @@ struct Cfg {
   static constexpr int kChunkBytes = 128 * 128;  // one atom column of a 128-row tile
   static constexpr int kQTile = kBM * D * 2;
   static constexpr int kKVTile = kBN * D * 2;
-  static constexpr int kPTile = kBM * kBN * 2;
-  static constexpr int kSlots = (D == 128) ? 3 : 8;
+  static constexpr int kSlots = (D == 128) ? 5 : 12;
   static constexpr int kOffQ0 = 0;
   static constexpr int kOffQ1 = kQTile;
-  static constexpr int kOffP0 = 2 * kQTile;
-  static constexpr int kOffP1 = 2 * kQTile + kPTile;
-  static constexpr int kOffKV = 2 * kQTile + 2 * kPTile;
+  static constexpr int kOffKV = 2 * kQTile;
   static constexpr int kOffBar = kOffKV + kSlots * kKVTile;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
+  static_assert(8 * (8 + 2 * kSlots) <= 496, "barriers overlap the TMEM slot");
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
 };
 
@@ -68,8 +71,8 @@ enum : int {
   kBarDrain = 7,
   kBarKVFull = 8,  // +slot; kv_empty follows the kv_full block
 };
-constexpr int kTmemSlotOff = 240;
-constexpr int kAbortOff = 244;
+constexpr int kTmemSlotOff = 496;
+constexpr int kAbortOff = 500;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns of S_i and O_i.
 __device__ __forceinline__ uint32_t col_s(int i) { return static_cast<uint32_t>(i) * 128u; }
@@ -101,6 +104,27 @@ __device__ __forceinline__ int causal_visible(int src, int64_t k0, int64_t gq, i
   return static_cast<int>(cntA + cntB);
 }
 
+// S_i = Q_i K^T over d: 16 columns of d per MMA; dq / dk are the tiles'
+// base descriptors, the k-step offset is added to the address field.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dq, uint64_t dk, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+    mma_ss(d_tmem, dq + off, dk + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O_i (+)= P_i V over 128 keys: P (bf16 pairs) from TMEM, 8 columns per
+// 16 keys; V MN-major, 16 keys = 2048 bytes per MMA.
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t dv,
+                                         uint32_t idesc, bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts(d_tmem, p_tmem + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc,
+           (acc || kk > 0) ? 1u : 0u);
+}
+
 struct Unit {
   int bh, g, rank, s_lo, s_hi, pair, part;
   int64_t q_row0;  // first row of the rank's query chunk in the Q tensor
@@ -130,13 +154,18 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams &p, int u) {
 struct TileIter {
   int s, t;
   int src;
+  __device__ __forceinline__ void init(const AttnParams &p, const Unit &w) {
+    s = w.s_lo;
+    t = 0;
+    src = ((w.rank - s) % p.P + p.P) % p.P;
+  }
   __device__ __forceinline__ void settle(const AttnParams &p, const Unit &w, int n_t,
                                          int64_t gq_max) {
     while (s < w.s_hi) {
-      src = ((w.rank - s) % p.P + p.P) % p.P;
       if (t >= n_t) {
         t = 0;
         ++s;
+        src = (src == 0) ? p.P - 1 : src - 1;  // next block in ring order
         continue;
       }
       if (p.causal) {
@@ -205,6 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Registers: the producer / MMA warpgroup gives most of its share to the
+  // two softmax warpgroups (128*80 + 256*208 <= 384*168, the launch total).
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
@@ -220,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t kv_base =
           static_cast<int64_t>(w.bh) * p.kv_rows_bh + static_cast<int64_t>(w.g) * p.kv_rows_g;
       int it = 0;
-      TileIter ti{w.s_lo, 0, 0};
+      TileIter ti;
+      ti.init(p, w);
       ti.settle(p, w, n_t, gq_max);
       bool ok = true;
       while (ok && ti.valid(w)) {
@@ -256,31 +290,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
       const uint32_t sQ[2] = {sbase + C::kOffQ0, sbase + C::kOffQ1};
-      const uint32_t sP[2] = {sbase + C::kOffP0, sbase + C::kOffP1};
       const int nq = has_q1 ? 2 : 1;
       bool issued = false;
-      TileIter ti{w.s_lo, 0, 0};
+      TileIter ti;
+      ti.init(p, w);
       ti.settle(p, w, n_t, gq_max);
-      // S_i = Q_i K^T over d: K-major operands, 16 columns of d per MMA.
+      const uint64_t dq[2] = {smem_desc_sw128(sbase + C::kOffQ0, 16, 1024),
+                              smem_desc_sw128(sbase + C::kOffQ1, 16, 1024)};
+      const uint64_t dk0 = smem_desc_sw128(sbase + C::kOffKV, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(sbase + C::kOffKV, C::kChunkBytes, 1024);
       auto issue_s = [&](int i, int slot) {
-        const uint32_t kb = sbase + C::kOffKV + slot * C::kKVTile;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + col_s(i), smem_desc_sw128(sQ[i] + off, 16, 1024),
-                 smem_desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-        }
+        issue_qk<D>(tmem + col_s(i), dq[i], dk0 + static_cast<uint64_t>(slot * (C::kKVTile >> 4)),
+                    idesc_s);
       };
-      // O_i (+)= P_i V over 128 keys: P K-major, V MN-major (d contiguous).
       auto issue_o = [&](int i, int slot, bool acc) {
-        const uint32_t vb = sbase + C::kOffKV + slot * C::kKVTile;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + col_o(i), smem_desc_sw128(sP[i] + aoff, 16, 1024),
-                 smem_desc_sw128(vb + kk * 2048, C::kChunkBytes, 1024), idesc_o,
-                 (acc || kk > 0) ? 1u : 0u);
-        }
+        issue_pv(tmem + col_o(i), tmem + col_s(i),
+                 dv0 + static_cast<uint64_t>(slot * (C::kKVTile >> 4)), idesc_o, acc);
       };
       if (ti.valid(w) && mbar_wait(bar0 + 8 * kBarQFull, 0, wd, abort_flag)) {
         tc_fence_after();
@@ -340,7 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(bar0 + 8 * kBarDrain, 0, p.wd.limit_ns);
       }
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;\n" ::: "memory");
     // ------------------------------------------------------------- softmax --
     const int wg = (warp - 4) >> 2;
     const int quarter = warp & 3;
@@ -349,18 +376,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
       const uint32_t tS = tmem + lane_bits + col_s(wg);
       const uint32_t tO = tmem + lane_bits + col_o(wg);
-      const uint32_t sP = sbase + (wg ? C::kOffP1 : C::kOffP0);
       const int64_t qi = pair_row0 + wg * kBM + row;  // row within the rank's chunk
       const bool row_valid = qi < p.L;
       const int64_t gq = p.causal ? zz_pos(w.rank, min64(qi, p.L - 1), half, p.P) : 0;
       const float sl2 = p.scale_log2;
-      // Row-invariant part of this row's swizzled P address.
-      const uint32_t p_row = sP + (row >> 3) * 1024 + (row & 7) * 128;
-      const int sw = row & 7;
 
       float m_ref = -INFINITY, l = 0.f;
       int j = 0;
-      TileIter ti{w.s_lo, 0, 0};
+      TileIter ti;
+      ti.init(p, w);
       ti.settle(p, w, n_t, gq_max);
       while (ti.valid(w)) {
         const bool ok =
@@ -381,10 +405,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kBN; ++c)
             if (c >= nvis) s[c] = -INFINITY;
         }
-        float mx = s[0];
+        // Row max with 3-input max (two new scores per instruction), 4 chains.
+        float mx[4];
 #pragma unroll
-        for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
-        const float mxs = mx * sl2;
+        for (int x = 0; x < 4; ++x) mx[x] = fmaxf(s[2 * x], s[2 * x + 1]);
+#pragma unroll
+        for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+          for (int x = 0; x < 4; ++x) mx[x] = fmax3(mx[x], s[c + 2 * x], s[c + 2 * x + 1]);
+        const float mxs = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
         float alpha = 1.f;
         bool rescale = false;
         if (mxs > m_ref + kRescaleThreshold) {
@@ -395,23 +424,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = mxs;
         }
         const float shift = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float rs = 0.f;
+        const float2 sl2v = make_float2(sl2, sl2);
+        const float2 nshift = make_float2(-shift, -shift);
+        float2 rs[4];
 #pragma unroll
-        for (int cc = 0; cc < kBN / 8; ++cc) {
-          float e[8];
+        for (int x = 0; x < 4; ++x) rs[x] = make_float2(0.f, 0.f);
+        // P overwrites the first 64 columns of this tile's S (already in
+        // registers): bf16 pairs, lower key in the low half.  Scale/shift and
+        // the row sum use packed f32x2 arithmetic (two scores per instruction).
 #pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            e[x] = ex2(fmaf(s[cc * 8 + x], sl2, -shift));
-            rs += e[x];
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            const float2 a = ffma2(make_float2(s[32 * c + 2 * x], s[32 * c + 2 * x + 1]), sl2v, nshift);
+            const float2 e = make_float2(ex2(a.x), ex2(a.y));
+            rs[x & 3] = fadd2(rs[x & 3], e);
+            pk[x] = pack_bf16x2(e.x, e.y);
           }
-          const uint32_t addr = p_row + (cc >> 3) * C::kChunkBytes + (((cc & 7) ^ sw) << 4);
-          st_shared_v4(addr, pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
-                       pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+          tmem_st16(tS + c * 16, pk);
         }
-        l = l * alpha + rs;
+        const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
+        const float2 r = fadd2(r01, r23);
+        const float rsum = r.x + r.y;
+        l = l * alpha + rsum;
         if (__any_sync(0xffffffffu, rescale)) {
-          // O holds the sum over earlier tiles (their PV finished before this
-          // tile's S was committed); scale it in place.
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
@@ -421,9 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int x = 0; x < 32; ++x) o[x] *= alpha;
             tmem_st32(tO + c * 32, o);
           }
-          tmem_wait_st();
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar0 + 8 * (kBarPFull + wg));
         ++j;
