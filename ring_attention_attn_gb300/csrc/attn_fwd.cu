@@ -14,8 +14,10 @@
 // CTA structure (384 threads, one CTA per SM, ~225 KB shared memory):
 //   warp 0       TMA producer: Q tile pair once, then K_j, V_j tiles through a
 //                ring of shared-memory slots (mbarrier full/empty pairs).
-//   warp 1       allocates 512 TMEM columns; one thread issues every
-//                tcgen05.mma and tcgen05.commit.
+//   warp 1       allocates 512 TMEM columns and issues every tcgen05.mma and
+//                tcgen05.commit: the whole warp runs the issue loop (so its
+//                operands stay warp-uniform) and one elected lane executes
+//                each tcgen05 instruction.
 //   warps 4..7   softmax for query tile 0 (one thread per query row),
 //   warps 8..11  softmax for query tile 1; the two tiles ping-pong so the
 //                tensor core computes one tile's PV / next QK^T while the
@@ -104,6 +106,7 @@ __device__ __forceinline__ int causal_visible(int src, int64_t k0, int64_t gq, i
   return static_cast<int>(cntA + cntB);
 }
 
+
 // S_i = Q_i K^T over d: 16 columns of d per MMA; dq / dk are the tiles'
 // base descriptors, the k-step offset is added to the address field.
 template <int D>
@@ -111,7 +114,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dq, uint64_t 
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-    mma_ss(d_tmem, dq + off, dk + off, idesc, kk > 0 ? 1u : 0u);
+    mma_ss_e(d_tmem, dq + off, dk + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -121,8 +124,8 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
                                          uint32_t idesc, bool acc) {
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    mma_ts(d_tmem, p_tmem + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc,
-           (acc || kk > 0) ? 1u : 0u);
+    mma_ts_e(d_tmem, p_tmem + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc,
+             (acc || kk > 0) ? 1u : 0u);
 }
 
 struct Unit {
@@ -286,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issue --
-    if (lane == 0) {
+    {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
       const uint32_t sQ[2] = {sbase + C::kOffQ0, sbase + C::kOffQ1};
@@ -315,9 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           for (int i = 0; i < nq; ++i) {
             issue_s(i, it % C::kSlots);
-            mma_commit(bar0 + 8 * (kBarSFull + i));
+            mma_commit_e(bar0 + 8 * (kBarSFull + i));
           }
-          mma_commit(kv_empty0 + 8 * (it % C::kSlots));
+          mma_commit_e(kv_empty0 + 8 * (it % C::kSlots));
           issued = true;
           ++it;
         }
@@ -339,29 +342,29 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             tc_fence_after();
             issue_s(0, k_it % C::kSlots);
-            mma_commit(bar0 + 8 * kBarSFull);
+            mma_commit_e(bar0 + 8 * kBarSFull);
           }
           if (has_q1) {
             if (!(ok = mbar_wait(bar0 + 8 * (kBarPFull + 1), j & 1, wd, abort_flag))) break;
             tc_fence_after();
             issue_o(1, v_it % C::kSlots, j > 0);
           }
-          mma_commit(kv_empty0 + 8 * (v_it % C::kSlots));
+          mma_commit_e(kv_empty0 + 8 * (v_it % C::kSlots));
           if (!more) break;
           if (has_q1) {
             issue_s(1, k_it % C::kSlots);
-            mma_commit(bar0 + 8 * (kBarSFull + 1));
+            mma_commit_e(bar0 + 8 * (kBarSFull + 1));
           }
-          mma_commit(kv_empty0 + 8 * (k_it % C::kSlots));
+          mma_commit_e(kv_empty0 + 8 * (k_it % C::kSlots));
           it = k_it + 1;
         }
         if (ok) {
-          for (int i = 0; i < nq; ++i) mma_commit(bar0 + 8 * (kBarODone + i));
+          for (int i = 0; i < nq; ++i) mma_commit_e(bar0 + 8 * (kBarODone + i));
         }
       }
       if (issued) {
         // Nothing may still be running on the tensor core when TMEM is freed.
-        mma_commit(bar0 + 8 * kBarDrain);
+        mma_commit_e(bar0 + 8 * kBarDrain);
         mbar_wait_drain(bar0 + 8 * kBarDrain, 0, p.wd.limit_ns);
       }
     }
