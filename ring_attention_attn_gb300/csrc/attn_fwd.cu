@@ -133,10 +133,25 @@ struct Unit {
   int64_t q_row0;  // first row of the rank's query chunk in the Q tensor
 };
 
+// When a rank's last query-tile pair holds a single tile (L mod 256 <= 128),
+// its units cost about half of the others; they are numbered last so that
+// the block scheduler, which hands out CTAs in index order, packs them into
+// the final, partial wave (longest units first).
 __device__ __forceinline__ Unit decode_unit(const AttnParams &p, int u) {
   Unit w;
-  w.pair = u % p.n_pairs;
-  u /= p.n_pairs;
+  int np = p.n_pairs, pair_base = 0;
+  if (p.n_pairs > 1 && p.L - static_cast<int64_t>(p.n_pairs - 1) * 2 * kBM <= kBM) {
+    const int heavy = (p.n_pairs - 1) * p.n_stepgroups * p.n_ranks * p.G * p.BH;
+    if (u < heavy) {
+      np = p.n_pairs - 1;
+    } else {
+      u -= heavy;
+      np = 1;
+      pair_base = p.n_pairs - 1;
+    }
+  }
+  w.pair = pair_base + u % np;
+  u /= np;
   w.part = u % p.n_stepgroups;
   u /= p.n_stepgroups;
   const int ri = u % p.n_ranks;
