@@ -300,6 +300,19 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
     p.kv_rows_bh = S;
     p.kv_rows_g = T;
     p.L = L;
+    if (L <= 128) {
+      // Short chunks: one 128-row tile carries the same rank's chunk of
+      // floor(128 / L) spatial positions (3-D TMA gather), each position's
+      // queries masked to its own keys.
+      const int pack = static_cast<int>(128 / L) < N ? static_cast<int>(128 / L) : N;
+      p.pack = pack;
+      p.Lf = static_cast<int>(L);
+      p.pN = N;
+      p.pT = T;
+      p.G = (N + pack - 1) / pack;
+      p.L = static_cast<int64_t>(pack) * L;
+      p.n_pairs = 1;
+    }
     p.P = P;
     p.steps_per_group = P;
     p.scale_log2 = scale_log2(d);

@@ -241,6 +241,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     mbar_fence_init();
   }
+  if (p.pack) {
+    // Rows past pack * Lf of the Q tile and of every K/V slot are never
+    // written by TMA: zero them once so that masked keys meet finite values
+    // (P = 0 times V must stay 0).
+    const int r0 = p.pack * p.Lf;
+    const int per_chunk = (kBM - r0) * 8;  // 16-byte units
+    const int regions = (C::kSlots + 1) * C::kChunks;
+    for (int idx = threadIdx.x; idx < regions * per_chunk; idx += kThreads) {
+      const int reg = idx / per_chunk, u = idx - reg * per_chunk;
+      const int slot = reg / C::kChunks, c = reg - slot * C::kChunks;
+      const uint32_t base = (slot < C::kSlots ? sbase + C::kOffKV + slot * C::kKVTile
+                                              : sbase + C::kOffQ0) + c * C::kChunkBytes;
+      st_shared_v4(base + r0 * 128 + u * 16, 0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+  }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
@@ -260,12 +276,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
       const uint32_t qfull = bar0 + 8 * kBarQFull;
-      const int32_t qy = static_cast<int32_t>(w.q_row0 + pair_row0);
-      mbar_arrive_expect_tx(qfull, 2 * C::kQTile);
+      // Packed mode: 3-D box {64 d, Lf rows, pack problems} starting at the
+      // rank's chunk of the unit's first problem.
+      const int32_t pz = static_cast<int32_t>(static_cast<int64_t>(w.bh) * p.pN +
+                                              static_cast<int64_t>(w.g) * p.pack);
+      const uint32_t pack_bytes = static_cast<uint32_t>(p.pack * p.Lf) * 128u * C::kChunks;
+      if (p.pack) {
+        mbar_arrive_expect_tx(qfull, pack_bytes);
 #pragma unroll
-      for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_2d(sbase + C::kOffQ0 + c * C::kChunkBytes, &tm_q, c * 64, qy, qfull);
-        tma_load_2d(sbase + C::kOffQ1 + c * C::kChunkBytes, &tm_q, c * 64, qy + kBM, qfull);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sbase + C::kOffQ0 + c * C::kChunkBytes, &tm_q, c * 64, w.rank * p.Lf, pz,
+                      qfull);
+      } else {
+        const int32_t qy = static_cast<int32_t>(w.q_row0 + pair_row0);
+        mbar_arrive_expect_tx(qfull, 2 * C::kQTile);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_2d(sbase + C::kOffQ0 + c * C::kChunkBytes, &tm_q, c * 64, qy, qfull);
+          tma_load_2d(sbase + C::kOffQ1 + c * C::kChunkBytes, &tm_q, c * 64, qy + kBM, qfull);
+        }
       }
       const uint64_t keep = l2_policy_evict_last();
       const int64_t kv_base =
@@ -286,12 +315,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(kv_full0 + 8 * slot, C::kKVTile);
           const CUtensorMap *map = which ? &tm_v : &tm_k;
+          if (p.pack) {
+            mbar_arrive_expect_tx(kv_full0 + 8 * slot, pack_bytes);
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d_hint(sbase + C::kOffKV + slot * C::kKVTile + c * C::kChunkBytes, map,
-                             c * 64, ky, kv_full0 + 8 * slot, keep);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(sbase + C::kOffKV + slot * C::kKVTile + c * C::kChunkBytes, map, c * 64,
+                          ti.src * p.Lf, pz, kv_full0 + 8 * slot);
+          } else {
+            mbar_arrive_expect_tx(kv_full0 + 8 * slot, C::kKVTile);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_2d_hint(sbase + C::kOffKV + slot * C::kKVTile + c * C::kChunkBytes, map,
+                               c * 64, ky, kv_full0 + 8 * slot, keep);
+          }
           ++it;
         }
         ++ti.t;
@@ -395,7 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tS = tmem + lane_bits + col_s(wg);
       const uint32_t tO = tmem + lane_bits + col_o(wg);
       const int64_t qi = pair_row0 + wg * kBM + row;  // row within the rank's chunk
-      const bool row_valid = qi < p.L;
+      // Packed mode: row qi is row qi % Lf of problem g * pack + qi / Lf and
+      // sees only the keys of that problem (columns [lo, lo + Lf) of a tile).
+      const int pr = p.pack ? static_cast<int>(qi / p.Lf) : 0;
+      const bool row_valid =
+          qi < p.L && (!p.pack || static_cast<int64_t>(w.g) * p.pack + pr < p.pN);
       const int64_t gq = p.causal ? zz_pos(w.rank, min64(qi, p.L - 1), half, p.P) : 0;
       const float sl2 = p.scale_log2;
 
@@ -418,10 +459,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t k0 = static_cast<int64_t>(ti.t) * kBN;
         int nvis = static_cast<int>(min64(kBN, p.L - k0));
         if (p.causal) nvis = causal_visible(ti.src, k0, gq, p.L, p.P);
-        if (nvis < kBN) {
+        int lo = 0;
+        if (p.pack) {
+          lo = pr * p.Lf;
+          nvis = min(nvis, lo + p.Lf);
+        }
+        if (lo > 0 || nvis < kBN) {
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
-            if (c >= nvis) s[c] = -INFINITY;
+            if (c < lo || c >= nvis) s[c] = -INFINITY;
         }
         // Row max with 3-input max (two new scores per instruction), 4 chains.
         float mx[4];
@@ -495,7 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!aborted) {
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
         const float lse_val = (l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
-        const int64_t orow = w.q_row0 + qi;
+        const int64_t orow =
+            p.pack ? (static_cast<int64_t>(w.bh) * p.pN + static_cast<int64_t>(w.g) * p.pack + pr) *
+                             p.pT + static_cast<int64_t>(w.rank) * p.Lf + (qi - static_cast<int64_t>(pr) * p.Lf)
+                   : w.q_row0 + qi;
         if (OUT_F32) {
           float *out = reinterpret_cast<float *>(p.out) + w.part * p.out_part_stride + orow * D;
 #pragma unroll
@@ -604,6 +653,24 @@ cudaError_t make_row_map(CUtensorMap *map, const void *base, int64_t rows, int d
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 3-D bf16 tensor [problems][rows][d]; box = 64 elements x Lf rows x pack
+// problems, 128-byte swizzle; coordinates past the end read as zero.
+cudaError_t make_pack_map(CUtensorMap *map, const void *base, int64_t problems, int rows, int Lf,
+                          int pack, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(problems)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(Lf), static_cast<cuuint32_t>(pack)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int D, bool OUT_F32>
 cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                            const AttnParams &p, int64_t n_units, cudaStream_t stream) {
@@ -634,9 +701,16 @@ cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k,
   if (n_units > 0x7fffffff) return cudaErrorInvalidConfiguration;
   CUtensorMap mq, mk, mv;
   cudaError_t e;
-  if ((e = make_row_map(&mq, q, q_total_rows, d)) != cudaSuccess) return e;
-  if ((e = make_row_map(&mk, k, kv_total_rows, d)) != cudaSuccess) return e;
-  if ((e = make_row_map(&mv, v, kv_total_rows, d)) != cudaSuccess) return e;
+  if (p.pack) {
+    const int64_t problems = static_cast<int64_t>(p.BH) * p.pN;
+    if ((e = make_pack_map(&mq, q, problems, p.pT, p.Lf, p.pack, d)) != cudaSuccess) return e;
+    if ((e = make_pack_map(&mk, k, problems, p.pT, p.Lf, p.pack, d)) != cudaSuccess) return e;
+    if ((e = make_pack_map(&mv, v, problems, p.pT, p.Lf, p.pack, d)) != cudaSuccess) return e;
+  } else {
+    if ((e = make_row_map(&mq, q, q_total_rows, d)) != cudaSuccess) return e;
+    if ((e = make_row_map(&mk, k, kv_total_rows, d)) != cudaSuccess) return e;
+    if ((e = make_row_map(&mv, v, kv_total_rows, d)) != cudaSuccess) return e;
+  }
   if (d == 128)
     return out_f32 ? launch_variant<128, true>(mq, mk, mv, p, n_units, stream)
                    : launch_variant<128, false>(mq, mk, mv, p, n_units, stream);

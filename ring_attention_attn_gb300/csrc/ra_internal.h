@@ -31,6 +31,12 @@ struct AttnParams {
   float *lse;
   int64_t out_part_stride;        // elements between step groups' outputs
   int64_t lse_part_stride;
+  // Packed short problems (temporal factored attention): when pack > 0 the
+  // Q/K/V tensors are [BH * pN problems][pT rows][d] and one tile holds the
+  // rank's chunk (Lf rows) of `pack` consecutive problems: L = pack * Lf,
+  // G = ceil(pN / pack), and a query only sees keys of its own problem.
+  int pack, Lf, pT;
+  int64_t pN;
   WatchdogParams wd;
 };
 
