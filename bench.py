@@ -56,6 +56,17 @@ def _dist_init(n):
     return rank, world, local
 
 
+def reduce_max_ms(ms, dist, device):
+    """Max of a per-rank time over all ranks (the job is as slow as its slowest
+    replica); identity without a process group."""
+    if dist is None:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -272,10 +283,7 @@ def run_ours(a, rank, world, local):
     status = ra.ra_get_status()
     if status != 0:
         raise RuntimeError(f"device status {status}")
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max_ms(total_ms, dist, dev)
 
     flops = acc.attention_flops(w.B * w.H, w.L, w.S, w.d)
     merge_bytes = acc.merge_bytes(n, w.B * w.H * w.L, w.d)
@@ -317,10 +325,8 @@ def run_ours(a, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) if e2e_steps else float("nan")
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    if e2e_steps:
+        e2e_ms = reduce_max_ms(e2e_ms, dist, dev)
     e2e_value = (world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12) if e2e_steps else None
     h2d = (q.numel() + k.numel() + v.numel()) * 2
     d2h = out.numel() * 2 + lse.numel() * 4
@@ -346,7 +352,7 @@ def run_ours(a, rank, world, local):
                          "traffic": _kernel_traffic("attn_fwd.cu", "ring_attn_kernel"),
                          "kernel": "ring_attn_kernel<128, fp32 partials>",
                          "peak_kind": f"bf16_tflops_sustained ({peaks['source']})"},
-            "merge": {"kernel": "lse_merge_kernel<128>", "bound": "hbm", "achieved": merge_gbs,
+            "merge": {"kernel": "lse_merge_kernel8<128, 1>", "bound": "hbm", "achieved": merge_gbs,
                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
                       "frac": merge_gbs / peaks["hbm_gbs"], "bytes_per_launch": merge_bytes,
                       "ms": merge_avg,
