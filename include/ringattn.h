@@ -103,6 +103,27 @@ int ring_attn_fwd_rank(const void *q_local, const void *k, const void *v, void *
                        float *lse_local, int B, int H, int64_t S, int d, int P, int rank,
                        int causal, int step_begin, int step_end, int out_fp32, void *stream);
 
+/* Ring attention with the K/V exchange performed as real copies, overlapped
+ * with the attention of the current step ("Because the sends overlap with
+ * compute on the current block, you can hide most of the communication
+ * latency", "day 83" blog, "Context parallelism: splitting the sequence";
+ * k8ai ring diagram: send next while computing current).  Same inputs,
+ * outputs and result as ring_attn_fwd.  Every simulated rank r owns a K/V
+ * double buffer in `workspace`; at step s the compute stream attends rank r's
+ * queries to the block in its current buffer (block (r - s) mod P) while
+ * `comm_stream` copies each rank's current block into the next buffer of rank
+ * r + 1 (2P device-to-device copies per step).  Each step writes fp32 partials
+ * (workspace), merged at the end by the lse_merge kernel on `stream`.
+ * comm_stream may equal stream (copies then serialise with compute).
+ * workspace: >= ring_attn_fwd_overlap_workspace(...) bytes, 256-byte aligned,
+ * used by this call only.  Events are created and released internally. */
+int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out, float *lse,
+                          int B, int H, int64_t S, int d, int P, int causal, void *workspace,
+                          size_t ws_bytes, void *stream, void *comm_stream);
+
+/* Workspace bytes of ring_attn_fwd_overlap (0 on bad arguments). */
+size_t ring_attn_fwd_overlap_workspace(int B, int H, int64_t S, int d, int P);
+
 /* Online-softmax merge of n normalised partials of the same rows ("the online
  * softmax trick", "day 83" blog, "Context parallelism: splitting the
  * sequence"):  M = max_i LSE_i,  w_i = exp(LSE_i - M),

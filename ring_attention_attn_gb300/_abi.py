@@ -23,7 +23,8 @@ ERRORS = {-1: "RA_ERR_ARG", -2: "RA_ERR_SHAPE", -3: "RA_ERR_ALIGN", -4: "RA_ERR_
 
 # Every symbol include/ringattn.h declares.
 EXPORTS = ("ra_cp_shard_index", "ra_ring_source", "ra_cp_shard", "ra_frame_transpose",
-           "ring_attn_fwd", "ring_attn_fwd_rank", "lse_merge", "factored_attn",
+           "ring_attn_fwd", "ring_attn_fwd_rank", "ring_attn_fwd_overlap",
+           "ring_attn_fwd_overlap_workspace", "lse_merge", "factored_attn",
            "factored_attn_workspace", "factored_attn_static", "ra_get_status",
            "ra_set_watchdog_ns",
            "ra_watchdog_selftest", "ra_strerror", "ra_last_cuda_error")
@@ -60,6 +61,9 @@ def lib():
                 "ring_attn_fwd": (i32, [vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, vp]),
                 "ring_attn_fwd_rank": (i32, [vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32,
                                              i32, i32, i32, i32, vp]),
+                "ring_attn_fwd_overlap": (i32, [vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32,
+                                                vp, sz, vp, vp]),
+                "ring_attn_fwd_overlap_workspace": (sz, [i32, i32, i64, i32, i32]),
                 "lse_merge": (i32, [vp, vp, i32, i64, i32, vp, vp, vp]),
                 "factored_attn": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                         vp, sz, vp]),
@@ -179,6 +183,31 @@ def ring_attn_fwd_rank(q_local, k, v, P: int, rank: int, causal: bool = False,
                                     _dev(out, odt, "out"), _dev(lse, torch.float32, "lse"), B, H,
                                     S, d, P, rank, int(causal), step_begin, step_end,
                                     int(out_fp32), _stream(stream)), "ring_attn_fwd_rank")
+    return out, lse
+
+
+def ring_attn_fwd_overlap_workspace(B: int, H: int, S: int, d: int, P: int) -> int:
+    return int(lib().ring_attn_fwd_overlap_workspace(B, H, S, d, P))
+
+
+def ring_attn_fwd_overlap(q, k, v, P: int, causal: bool = False, workspace=None, out=None,
+                          lse=None, stream=None, comm_stream=None):
+    """ring_attn_fwd with the ring's K/V exchange done as device copies on
+    `comm_stream`, overlapped with each step's attention (sharded order)."""
+    import torch
+    B, H, S, d = q.shape
+    need = ring_attn_fwd_overlap_workspace(B, H, S, d, P)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    comm = _stream(comm_stream) if comm_stream is not None else None
+    _check(lib().ring_attn_fwd_overlap(_dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"),
+                                       _dev(v, torch.bfloat16, "v"),
+                                       _dev(out, torch.bfloat16, "out"),
+                                       _dev(lse, torch.float32, "lse"), B, H, S, d, P, int(causal),
+                                       _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                       _stream(stream), comm), "ring_attn_fwd_overlap")
     return out, lse
 
 

@@ -209,6 +209,130 @@ int ring_attn_fwd_rank(const void *q_local, const void *k, const void *v, void *
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
 
+// Workspace of ring_attn_fwd_overlap: two K/V buffers of [P][BH][L][d] bf16
+// each (K then V), then fp32 partials [P][BH][S][d] and LSEs [P][BH][S].
+static size_t ovl_part(size_t bytes) { return (bytes + 255) & ~static_cast<size_t>(255); }
+
+size_t ring_attn_fwd_overlap_workspace(int B, int H, int64_t S, int d, int P) {
+  if (B < 0 || H < 0 || S < 0 || P <= 0 || check_d(d) != RA_OK) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * S;
+  return 4 * ovl_part(rows * d * 2) + ovl_part(static_cast<size_t>(P) * rows * d * 4) +
+         ovl_part(static_cast<size_t>(P) * rows * 4);
+}
+
+int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out, float *lse,
+                          int B, int H, int64_t S, int d, int P, int causal, void *workspace,
+                          size_t ws_bytes, void *stream, void *comm_stream) {
+  if (B < 0 || H < 0 || S < 0 || P <= 0 || P > 64 || (causal != 0 && causal != 1))
+    return RA_ERR_ARG;
+  if (check_d(d) != RA_OK || S % P != 0) return RA_ERR_SHAPE;
+  if (causal && S % (2 * static_cast<int64_t>(P)) != 0) return RA_ERR_SHAPE;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH == 0 || S == 0) return RA_OK;
+  if (!q || !k || !v || !out || !lse) return RA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return RA_ERR_ALIGN;
+  if (BH * S > kMaxRows || BH > 0x7fffffff) return RA_ERR_SHAPE;
+  const size_t need = ring_attn_fwd_overlap_workspace(B, H, S, d, P);
+  if (!workspace || ws_bytes < need) return RA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RA_ERR_ALIGN;
+  cudaStream_t cs = as_stream(stream);
+  cudaStream_t xs = comm_stream ? as_stream(comm_stream) : cs;
+  ra::WatchdogParams wd;
+  if (!watchdog(&wd)) return fail_cuda(cudaGetLastError());
+
+  const int64_t L = S / P;
+  const size_t blk_bytes = static_cast<size_t>(BH * L) * d * 2;  // one rank's block, one tensor
+  const size_t buf_bytes = ovl_part(static_cast<size_t>(BH * S) * d * 2);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  uint8_t *kb[2] = {ws, ws + 2 * buf_bytes};
+  uint8_t *vb[2] = {ws + buf_bytes, ws + 3 * buf_bytes};
+  float *o_parts = reinterpret_cast<float *>(ws + 4 * buf_bytes);
+  float *l_parts = reinterpret_cast<float *>(
+      ws + 4 * buf_bytes + ovl_part(static_cast<size_t>(P) * BH * S * d * 4));
+
+  cudaEvent_t copied[2], consumed[2];
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 2; ++i) {
+    if ((e = cudaEventCreateWithFlags(&copied[i], cudaEventDisableTiming)) != cudaSuccess)
+      return fail_cuda(e);
+    if ((e = cudaEventCreateWithFlags(&consumed[i], cudaEventDisableTiming)) != cudaSuccess)
+      return fail_cuda(e);
+  }
+  // The comm stream may not start before inputs written on `stream` are ready.
+  cudaEvent_t start;
+  if ((e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming)) != cudaSuccess)
+    return fail_cuda(e);
+  e = cudaEventRecord(start, cs);
+  if (e == cudaSuccess && xs != cs) e = cudaStreamWaitEvent(xs, start, 0);
+
+  for (int s = 0; s < P && e == cudaSuccess; ++s) {
+    // ---- comm: ring send for step s + 1 (rank r receives rank r-1's block).
+    if (s + 1 < P) {
+      const int nb = (s + 1) & 1;
+      if (s >= 1) e = cudaStreamWaitEvent(xs, consumed[nb], 0);  // step s-1 read it
+      for (int r = 0; r < P && e == cudaSuccess; ++r) {
+        const int from = (r + P - 1) % P;
+        for (int t = 0; t < 2 && e == cudaSuccess; ++t) {
+          uint8_t *dst = (t ? vb[nb] : kb[nb]) + static_cast<size_t>(r) * blk_bytes;
+          if (s == 0) {
+            const uint8_t *src = static_cast<const uint8_t *>(t ? v : k) +
+                                 static_cast<size_t>(from * L) * d * 2;
+            e = cudaMemcpy2DAsync(dst, static_cast<size_t>(L) * d * 2, src,
+                                  static_cast<size_t>(S) * d * 2, static_cast<size_t>(L) * d * 2,
+                                  static_cast<size_t>(BH), cudaMemcpyDeviceToDevice, xs);
+          } else {
+            const uint8_t *src = (t ? vb[s & 1] : kb[s & 1]) + static_cast<size_t>(from) * blk_bytes;
+            e = cudaMemcpyAsync(dst, src, blk_bytes, cudaMemcpyDeviceToDevice, xs);
+          }
+        }
+      }
+      if (e == cudaSuccess) e = cudaEventRecord(copied[nb], xs);
+    }
+    if (e != cudaSuccess) break;
+    // ---- compute: step s for every rank, from its current buffer.
+    if (s >= 1) e = cudaStreamWaitEvent(cs, copied[s & 1], 0);
+    if (e != cudaSuccess) break;
+    ra::AttnParams p{};
+    p.BH = static_cast<int>(BH);
+    p.G = 1;
+    p.n_ranks = P;
+    p.n_stepgroups = 1;
+    p.n_pairs = static_cast<int>((L + 255) / 256);
+    p.q_rows_bh = S;
+    p.L = L;
+    p.P = P;
+    p.step_begin = s;
+    p.steps_per_group = 1;
+    p.causal = causal;
+    p.scale_log2 = scale_log2(d);
+    p.out = o_parts + static_cast<size_t>(s) * BH * S * d;
+    p.lse = l_parts + static_cast<size_t>(s) * BH * S;
+    p.wd = wd;
+    const void *ks = k, *vs = v;
+    int64_t kv_rows = BH * S;
+    if (s == 0) {
+      p.kv_rows_bh = S;
+    } else {
+      p.kv_own = 1;
+      p.kv_rows_bh = L;
+      p.kv_rank_stride = BH * L;
+      ks = kb[s & 1];
+      vs = vb[s & 1];
+    }
+    e = ra::launch_ring_attn(q, BH * S, ks, vs, kv_rows, d, true, p, cs);
+    if (e == cudaSuccess && s >= 1) e = cudaEventRecord(consumed[s & 1], cs);
+  }
+  if (e == cudaSuccess)
+    e = ra::launch_lse_merge(o_parts, l_parts, P, BH * S, d, out, lse, cs);
+  for (int i = 0; i < 2; ++i) {
+    cudaEventDestroy(copied[i]);
+    cudaEventDestroy(consumed[i]);
+  }
+  cudaEventDestroy(start);
+  return e == cudaSuccess ? RA_OK : fail_cuda(e);
+}
+
 int lse_merge(const float *o_parts, const float *lse_parts, int n, int64_t rows, int d, void *out,
               float *lse_out, void *stream) {
   if (n < 1 || n > 64 || rows < 0) return RA_ERR_ARG;

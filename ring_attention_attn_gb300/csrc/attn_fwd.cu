@@ -305,8 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ti.settle(p, w, n_t, gq_max);
       bool ok = true;
       while (ok && ti.valid(w)) {
-        const int32_t ky = static_cast<int32_t>(kv_base + static_cast<int64_t>(ti.src) * p.L +
-                                                static_cast<int64_t>(ti.t) * kBN);
+        const int64_t blk = p.kv_own ? static_cast<int64_t>(w.rank) * p.kv_rank_stride +
+                                           static_cast<int64_t>(w.bh) * p.kv_rows_bh
+                                     : kv_base + static_cast<int64_t>(ti.src) * p.L;
+        const int32_t ky = static_cast<int32_t>(blk + static_cast<int64_t>(ti.t) * kBN);
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           const int slot = it % C::kSlots;

@@ -37,6 +37,11 @@ struct AttnParams {
   // G = ceil(pN / pack), and a query only sees keys of its own problem.
   int pack, Lf, pT;
   int64_t pN;
+  // Per-rank K/V buffers (overlapped ring): when kv_own != 0, rank r's
+  // current block for head bh is rows [r * kv_rank_stride + bh * kv_rows_bh,
+  // + L) of the K/V tensors, whatever block of the ring it holds.
+  int kv_own;
+  int64_t kv_rank_stride;
   WatchdogParams wd;
 };
 

@@ -215,6 +215,26 @@ def test_c5_full_size_sampled():
     assert (o.float() - fo.float()).abs().max().item() <= 2e-3
 
 
+# ------------------------------------------------- overlapped ring copies --
+@pytest.mark.parametrize("B,H,S,d,P,causal,separate",
+                         [(1, 2, 2048, 128, 4, False, True), (1, 2, 4096, 64, 2, True, True),
+                          (2, 1, 1200, 128, 3, True, False), (1, 3, 1000, 64, 8, False, True)])
+def test_overlap_ring_matches_oracle_and_fused(B, H, S, d, P, causal, separate):
+    layout = 1 if causal else 0
+    q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=S + 11 * P + causal)
+    qs, ks, vs = (_shard_host(x, P, layout).cuda() for x in (q, k, v))
+    comm = torch.cuda.Stream() if separate else None
+    o, l = ra.ring_attn_fwd_overlap(qs, ks, vs, P, causal=causal, comm_stream=comm)
+    fo, fl = ra.ring_attn_fwd(qs, ks, vs, P, causal=causal)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+    assert (o.float() - fo.float()).abs().max().item() <= 4e-3
+    assert (l - fl).abs().max().item() <= 1e-4
+    ro, rl = oracle.attention(q, k, v, causal=causal)
+    _cmp(_unshard_host(o.cpu(), P, layout), _unshard_host(l.cpu().unsqueeze(-1), P, layout).squeeze(-1),
+         ro, rl)
+
+
 # ---------------------------------------------------------------- factored --
 def test_factored_small_full():
     B, H, T, N, d, P = 1, 2, 8, 50, 64, 4
