@@ -17,7 +17,11 @@ Citations (page title, section):
   * balanced causal chunking -- k8ai, "How context parallel works", read as
     zigzag (2P chunks, rank r holds chunks r and 2P-1-r);
   * factored spatial / temporal attention -- "day 83" blog, "The
-    spatial-temporal twist".
+    spatial-temporal twist";
+  * the backward pass ("Ring exchanges happen in every attention layer,
+    forward and backward", k8ai "Communication profile"; the glossary's
+    example calls .backward()) -- the gradients of the full-attention
+    definition.
 """
 from __future__ import annotations
 
@@ -61,6 +65,8 @@ def configure(lib):
     lib.oracle_ring_attention.argtypes = [vp, vp, vp, i64, i64, i64, i64, i32, vp, vp, i64, vp,
                                           vp]
     lib.oracle_lse_merge.argtypes = [vp, vp, i64, i64, i64, vp, vp]
+    lib.oracle_attention_bwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp, vp, vp]
+    lib.oracle_attention_bwd.restype = i32
     lib.oracle_ring_source.argtypes = [i64, i64, i64]
     lib.oracle_ring_source.restype = i64
     for f in ("oracle_shard_index", "oracle_attention", "oracle_factored",
@@ -195,6 +201,24 @@ def ring_attention(q, k, v, P: int, causal: bool = False, order=None, rows=None)
     if r is None:
         return o.reshape(B, H, S, d), lse.reshape(B, H, S)
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, causal: bool = False):
+    """fp64 gradients (dq, dk, dv) of full attention for upstream gradient dout.
+
+    q, k, v, dout: [B,H,S,d] bf16 in global order; returns float64 arrays of
+    the same shape.
+    """
+    B, H, S, d = q.shape
+    qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(dout)
+    dq = np.empty((B, H, S, d))
+    dk = np.empty((B, H, S, d))
+    dv = np.empty((B, H, S, d))
+    rc = _load().oracle_attention_bwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), B * H, S, d,
+                                      int(causal), _ptr(dq), _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise MemoryError("oracle_attention_bwd failed")
+    return dq, dk, dv
 
 
 def lse_merge(o_parts, lse_parts):

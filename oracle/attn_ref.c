@@ -267,6 +267,72 @@ int oracle_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t *
     return 0;
 }
 
+/* ----------------------------------------------------------- backward -- */
+
+/* Gradients of full attention (the definition, differentiated):
+ *   s_ij = scale q_i.k_j,  P_ij = exp(s_ij - LSE_i),  O_i = sum_j P_ij v_j
+ *   dV_j = sum_i P_ij dO_i
+ *   dP_ij = dO_i . v_j,   D_i = sum_j P_ij dP_ij  (= dO_i . O_i)
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i
+ * K(i) as in oracle_attention (causal: j <= i).  All of [BH, S, d] in global
+ * order; dq/dk/dv: [BH, S, d] fp64 outputs.  Parallel over heads. */
+int oracle_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const uint16_t *dout, int64_t BH, int64_t S, int64_t d, int causal,
+                         double *dq, double *dk, double *dv)
+{
+    double scale = 1.0 / sqrt((double)d);
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        const uint16_t *Q = q + bh * S * d, *K = k + bh * S * d, *V = v + bh * S * d;
+        const uint16_t *dO = dout + bh * S * d;
+        double *dQ = dq + bh * S * d, *dK = dk + bh * S * d, *dV = dv + bh * S * d;
+        double *P = (double *)malloc(sizeof(double) * (size_t)(S ? S : 1));
+        double *dP = (double *)malloc(sizeof(double) * (size_t)(S ? S : 1));
+        if (!P || !dP) {
+#pragma omp atomic write
+            bad = 1;
+            free(P);
+            free(dP);
+            continue;
+        }
+        for (int64_t x = 0; x < S * d; ++x) dQ[x] = dK[x] = dV[x] = 0.0;
+        for (int64_t i = 0; i < S; ++i) {
+            int64_t n = causal ? i + 1 : S;
+            double m = -INFINITY;
+            for (int64_t j = 0; j < n; ++j) {
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c) dot += widen_bf16(Q[i * d + c]) * widen_bf16(K[j * d + c]);
+                P[j] = dot * scale;
+                if (P[j] > m) m = P[j];
+            }
+            double z = 0.0;
+            for (int64_t j = 0; j < n; ++j) z += exp(P[j] - m);
+            double lse = m + log(z);
+            double D = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                P[j] = exp(P[j] - lse);
+                double t = 0.0;
+                for (int64_t c = 0; c < d; ++c) t += widen_bf16(dO[i * d + c]) * widen_bf16(V[j * d + c]);
+                dP[j] = t;
+                D += P[j] * t;
+            }
+            for (int64_t j = 0; j < n; ++j) {
+                double ds = P[j] * (dP[j] - D);
+                for (int64_t c = 0; c < d; ++c) {
+                    dV[j * d + c] += P[j] * widen_bf16(dO[i * d + c]);
+                    dQ[i * d + c] += scale * ds * widen_bf16(K[j * d + c]);
+                    dK[j * d + c] += scale * ds * widen_bf16(Q[i * d + c]);
+                }
+            }
+        }
+        free(P);
+        free(dP);
+    }
+    return bad ? -1 : 0;
+}
+
 /* -------------------------------------------------------------- merge ---- */
 
 /* Merge n normalised partials (O_i, LSE_i) of the same rows.

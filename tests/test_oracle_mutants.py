@@ -13,6 +13,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_bwd as bwd
 import test_oracle_pins as pins
 import test_page_figures as figures
 
@@ -40,6 +41,14 @@ MUTANTS = {
                             "int64_t chunk = (i < C) ? r : (P + r);",
                             [lambda: pins.test_zigzag_is_a_permutation_with_two_chunks_per_rank(48, 4),
                              pins.test_zigzag_balances_causal_work]),
+    "bwd_ds_drops_d": ("double ds = P[j] * (dP[j] - D);", "double ds = P[j] * dP[j];",
+                       [lambda: bwd.test_against_torch_float64_autograd(False)]),
+    "bwd_dk_unscaled": ("dK[j * d + c] += scale * ds * widen_bf16(Q[i * d + c]);",
+                        "dK[j * d + c] += ds * widen_bf16(Q[i * d + c]);",
+                        [lambda: bwd.test_finite_differences_against_brute_force(False)]),
+    "bwd_dv_from_dp": ("dV[j * d + c] += P[j] * widen_bf16(dO[i * d + c]);",
+                       "dV[j * d + c] += dP[j] * widen_bf16(dO[i * d + c]);",
+                       [lambda: bwd.test_finite_differences_against_brute_force(True)]),
     "temporal_stride_wrong": ("attend(q + flat * d, Kh, Vh, d, pos, T, N, scale",
                               "attend(q + flat * d, Kh, Vh, d, pos, T, 1, scale",
                               [pins.test_factored_temporal_across_frames]),
