@@ -124,6 +124,26 @@ int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out
 /* Workspace bytes of ring_attn_fwd_overlap (0 on bad arguments). */
 size_t ring_attn_fwd_overlap_workspace(int B, int H, int64_t S, int d, int P);
 
+/* Backward pass of ring_attn_fwd ("Ring exchanges happen in every attention
+ * layer, forward and backward", k8ai "Sequence and Context Parallel",
+ * "Communication profile").  Gradients of the loss with upstream gradient
+ * dout = dL/dO:  P_ij = exp(q_i.k_j / sqrt(d) - LSE_i),  D_i = dO_i . O_i,
+ *   dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (dO_i . v_j - D_i),
+ *   dQ_i = sum_j dS_ij k_j / sqrt(d),  dK_j = sum_i dS_ij q_i / sqrt(d).
+ * q, k, v, out (the forward output), dout, dq, dk, dv: bf16 [B, H, S, d] and
+ * lse (the forward LSE): fp32 [B, H, S], all in sharded order with the same
+ * P and causal flag as the forward.  Rank r's dQ visits the K/V blocks in the
+ * forward's ring order; block b's dK/dV gather the query chunks of ranks
+ * b, b+1, ... (the order the block travels the ring).  workspace: at least
+ * ring_attn_bwd_workspace(...) bytes (fp32 D), 256-byte aligned, used by this
+ * call only.  dq, dk, dv must not overlap the inputs. */
+int ring_attn_bwd(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                  const void *dout, void *dq, void *dk, void *dv, int B, int H, int64_t S, int d,
+                  int P, int causal, void *workspace, size_t ws_bytes, void *stream);
+
+/* Workspace bytes of ring_attn_bwd (0 on bad arguments). */
+size_t ring_attn_bwd_workspace(int B, int H, int64_t S);
+
 /* Online-softmax merge of n normalised partials of the same rows ("the online
  * softmax trick", "day 83" blog, "Context parallelism: splitting the
  * sequence"):  M = max_i LSE_i,  w_i = exp(LSE_i - M),

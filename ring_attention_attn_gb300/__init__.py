@@ -21,6 +21,8 @@ from ._abi import (  # noqa: F401
     ra_set_watchdog_ns,
     ra_watchdog_selftest,
     ring_attn_fwd,
+    ring_attn_bwd,
+    ring_attn_bwd_workspace,
     ring_attn_fwd_overlap,
     ring_attn_fwd_overlap_workspace,
     ring_attn_fwd_rank,

@@ -24,7 +24,8 @@ ERRORS = {-1: "RA_ERR_ARG", -2: "RA_ERR_SHAPE", -3: "RA_ERR_ALIGN", -4: "RA_ERR_
 # Every symbol include/ringattn.h declares.
 EXPORTS = ("ra_cp_shard_index", "ra_ring_source", "ra_cp_shard", "ra_frame_transpose",
            "ring_attn_fwd", "ring_attn_fwd_rank", "ring_attn_fwd_overlap",
-           "ring_attn_fwd_overlap_workspace", "lse_merge", "factored_attn",
+           "ring_attn_fwd_overlap_workspace", "ring_attn_bwd", "ring_attn_bwd_workspace",
+           "lse_merge", "factored_attn",
            "factored_attn_workspace", "factored_attn_static", "ra_get_status",
            "ra_set_watchdog_ns",
            "ra_watchdog_selftest", "ra_strerror", "ra_last_cuda_error")
@@ -64,6 +65,9 @@ def lib():
                 "ring_attn_fwd_overlap": (i32, [vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32,
                                                 vp, sz, vp, vp]),
                 "ring_attn_fwd_overlap_workspace": (sz, [i32, i32, i64, i32, i32]),
+                "ring_attn_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32, i32,
+                                        i32, vp, sz, vp]),
+                "ring_attn_bwd_workspace": (sz, [i32, i32, i64]),
                 "lse_merge": (i32, [vp, vp, i32, i64, i32, vp, vp, vp]),
                 "factored_attn": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                         vp, sz, vp]),
@@ -209,6 +213,31 @@ def ring_attn_fwd_overlap(q, k, v, P: int, causal: bool = False, workspace=None,
                                        _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
                                        _stream(stream), comm), "ring_attn_fwd_overlap")
     return out, lse
+
+
+def ring_attn_bwd_workspace(B: int, H: int, S: int) -> int:
+    return int(lib().ring_attn_bwd_workspace(B, H, S))
+
+
+def ring_attn_bwd(q, k, v, out, lse, dout, P: int, causal: bool = False, workspace=None,
+                  grads=None, stream=None):
+    """Gradients (dq, dk, dv) of ring_attn_fwd for upstream gradient dout
+    (all [B,H,S,d] bf16, sharded order; lse fp32 [B,H,S] from the forward)."""
+    import torch
+    B, H, S, d = q.shape
+    need = ring_attn_bwd_workspace(B, H, S)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = grads if grads is not None else (torch.empty_like(q), torch.empty_like(k),
+                                                  torch.empty_like(v))
+    bf = torch.bfloat16
+    _check(lib().ring_attn_bwd(_dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"),
+                               _dev(out, bf, "out"), _dev(lse, torch.float32, "lse"),
+                               _dev(dout, bf, "dout"), _dev(dq, bf, "dq"), _dev(dk, bf, "dk"),
+                               _dev(dv, bf, "dv"), B, H, S, d, P, int(causal),
+                               _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                               _stream(stream)), "ring_attn_bwd")
+    return dq, dk, dv
 
 
 def lse_merge(o_parts, lse_parts, out=None, lse_out=None, stream=None):

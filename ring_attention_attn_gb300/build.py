@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libringattn.so")
-SOURCES = ["api.cu", "attn_fwd.cu", "merge.cu", "noalloc.cu", "shard.cu"]
+SOURCES = ["api.cu", "attn_bwd.cu", "attn_fwd.cu", "merge.cu", "noalloc.cu", "shard.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

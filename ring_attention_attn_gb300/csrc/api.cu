@@ -333,6 +333,45 @@ int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
 
+size_t ring_attn_bwd_workspace(int B, int H, int64_t S) {
+  if (B < 0 || H < 0 || S < 0) return 0;
+  return ovl_part(static_cast<size_t>(B) * H * S * 4);
+}
+
+int ring_attn_bwd(const void *q, const void *k, const void *v, const void *out, const float *lse,
+                  const void *dout, void *dq, void *dk, void *dv, int B, int H, int64_t S, int d,
+                  int P, int causal, void *workspace, size_t ws_bytes, void *stream) {
+  if (B < 0 || H < 0 || S < 0 || P <= 0 || (causal != 0 && causal != 1)) return RA_ERR_ARG;
+  if (check_d(d) != RA_OK || S % P != 0) return RA_ERR_SHAPE;
+  if (causal && S % (2 * static_cast<int64_t>(P)) != 0) return RA_ERR_SHAPE;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH == 0 || S == 0) return RA_OK;
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return RA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return RA_ERR_ALIGN;
+  if (BH * S > kMaxRows || BH > 0x7fffffff) return RA_ERR_SHAPE;
+  if (!workspace || ws_bytes < ring_attn_bwd_workspace(B, H, S)) return RA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RA_ERR_ALIGN;
+  ra::BwdParams p{};
+  p.BH = static_cast<int>(BH);
+  p.P = P;
+  p.S = S;
+  p.L = S / P;
+  p.n_t = static_cast<int>((p.L + 127) / 128);
+  p.causal = causal;
+  p.scale_log2 = scale_log2(d);
+  p.scale = static_cast<float>(1.0 / sqrt(static_cast<double>(d)));
+  p.lse = lse;
+  p.Dv = static_cast<float *>(workspace);
+  p.dq = static_cast<__nv_bfloat16 *>(dq);
+  p.dk = static_cast<__nv_bfloat16 *>(dk);
+  p.dv = static_cast<__nv_bfloat16 *>(dv);
+  if (!watchdog(&p.wd)) return fail_cuda(cudaGetLastError());
+  cudaError_t e = ra::launch_attn_bwd(q, k, v, out, dout, d, p, as_stream(stream));
+  return e == cudaSuccess ? RA_OK : fail_cuda(e);
+}
+
 int lse_merge(const float *o_parts, const float *lse_parts, int n, int64_t rows, int d, void *out,
               float *lse_out, void *stream) {
   if (n < 1 || n > 64 || rows < 0) return RA_ERR_ARG;

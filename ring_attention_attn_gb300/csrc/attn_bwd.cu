@@ -1,0 +1,624 @@
+// Ring-attention backward for sm_103a: gradients dQ, dK, dV of the forward
+// in attn_fwd.cu ("Ring exchanges happen in every attention layer, forward
+// and backward", k8ai "Sequence and Context Parallel", "Communication
+// profile").  With s_ij = scale q_i.k_j, P_ij = exp(s_ij - LSE_i) (LSE from
+// the forward) and D_i = dO_i . O_i:
+//     dP_ij = dO_i . v_j,   dS_ij = P_ij (dP_ij - D_i),
+//     dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,
+//     dQ_i = scale sum_j dS_ij k_j.
+// The ring order is kept: rank r's dQ visits K/V blocks (r - s) mod P at
+// step s, as in the forward; block b's dK/dV gather the query chunks of the
+// ranks the block passes through, r = (b + s) mod P at step s.
+//
+// Three kernels:
+//   bwd_prep_kernel   D_i = dO_i . O_i (fp32), one warp per row.
+//   bwd_dq_kernel     one 128-row query tile per CTA.  Per K/V tile:
+//                     S = Q K^T and dP = dO V^T (SMEM operands) into TMEM;
+//                     the compute warpgroup writes dS (bf16) over S's first 64
+//                     columns; dQ += dS K takes dS from TMEM.
+//   bwd_dkv_kernel    one 128-key tile per CTA.  Per query tile:
+//                     S^T = K Q^T and dP^T = V dO^T; the compute warpgroup
+//                     writes P^T over S^T and dS^T over dP^T (bf16);
+//                     dV += P^T dO and dK += dS^T Q take them from TMEM.
+// Roles (256 threads): warp 0 TMA producer, warp 1 TMEM allocation and
+// elected MMA issue, warps 4..7 one thread per row of the tile.
+#include <math.h>
+
+#include "attn_common.cuh"
+#include "ra_device.cuh"
+#include "ra_internal.h"
+
+namespace ra {
+namespace {
+
+constexpr int kThreadsB = 256;
+constexpr float kLog2eB = 1.44269504088896340736f;
+
+constexpr int kBKVFirst = 8;
+
+template <int D>
+struct BCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kChunkBytes = 128 * 128;
+  static constexpr int kTile = 128 * D * 2;
+  // as many streamed-tile slots as fit next to the two fixed tiles
+  static constexpr int kSlots = (232448 - 1024 - 512 - 2048 - 2 * kTile) / kTile;
+  static constexpr int kOffA = 0;           // Q (dQ kernel) or K (dK/dV kernel)
+  static constexpr int kOffB = kTile;       // dO (dQ kernel) or V (dK/dV kernel)
+  static constexpr int kOffKV = 2 * kTile;  // ring of streamed tiles
+  static constexpr int kOffBar = kOffKV + kSlots * kTile;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kOffLD = kOffBar + kBarBytes;  // 2 x (LSE[128], D[128]) fp32
+  static constexpr int kLDBytes = 2048;
+  static constexpr int kSmemBytes = kOffLD + kLDBytes + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(8 * (kBKVFirst + 2 * kSlots) <= 496, "barriers overlap the TMEM slot");
+};
+
+enum : int { kBA = 0, kBS = 1, kBP = 2, kBO = 3, kBDrain = 4, kBLd = 5, kBKV = 8 };  // kBLd: +0/+1
+constexpr int kBTmemSlot = 496;
+constexpr int kBAbort = 500;
+constexpr uint32_t kColS = 0, kColP = 128, kColAcc0 = 256, kColAcc1 = 384;
+
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ out,
+                                                       const __nv_bfloat16 *__restrict__ dout,
+                                                       float *__restrict__ Dv, int64_t rows, int d) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (row >= rows) return;
+  float acc = 0.f;
+  for (int c = lane * 2; c < d; c += 64) {
+    const __nv_bfloat162 o = *reinterpret_cast<const __nv_bfloat162 *>(out + row * d + c);
+    const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162 *>(dout + row * d + c);
+    acc = fmaf(__low2float(o), __low2float(g), acc);
+    acc = fmaf(__high2float(o), __high2float(g), acc);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) Dv[row] = acc;
+}
+
+// K/V blocks for rank r (dQ) or query chunks for block b (dK/dV), in ring
+// order, in 128-row tiles; causal tiles with nothing visible are skipped.
+struct BIter {
+  int s, t, blk;
+  int P, n_t, causal, dir;  // dir -1: blk = (r - s) mod P; +1: blk = (b + s) mod P
+  int64_t C, limit;         // causal: dQ skips tiles with min position > limit,
+                            //         dK/dV skips tiles with max position < limit
+  int64_t L;
+  __device__ __forceinline__ void settle() {
+    while (s < P) {
+      if (t >= n_t) {
+        t = 0;
+        ++s;
+        blk = dir < 0 ? (blk == 0 ? P - 1 : blk - 1) : (blk == P - 1 ? 0 : blk + 1);
+        continue;
+      }
+      if (causal) {
+        const int64_t t0 = static_cast<int64_t>(t) * 128;
+        const bool skip = dir < 0 ? zz_pos(blk, t0, C, P) > limit
+                                  : zz_pos(blk, min64(t0 + 127, L - 1), C, P) < limit;
+        if (skip) {
+          ++t;
+          continue;
+        }
+      }
+      return;
+    }
+  }
+  __device__ __forceinline__ bool valid() const { return s < P; }
+};
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const float (&o)[32], float mul) {
+  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+    d4[x] = make_uint4(pack_bf16x2(o[8 * x] * mul, o[8 * x + 1] * mul),
+                       pack_bf16x2(o[8 * x + 2] * mul, o[8 * x + 3] * mul),
+                       pack_bf16x2(o[8 * x + 4] * mul, o[8 * x + 5] * mul),
+                       pack_bf16x2(o[8 * x + 6] * mul, o[8 * x + 7] * mul));
+}
+
+// One barrier-block layout for both kernels.
+struct BBars {
+  uint32_t bar0, kv_full0, kv_empty0;
+  __device__ __forceinline__ uint32_t b(int i) const { return bar0 + 8 * i; }
+};
+
+template <int D>
+__device__ __forceinline__ BBars init_bars(uint32_t sbase) {
+  using C = BCfg<D>;
+  BBars r;
+  r.bar0 = sbase + C::kOffBar;
+  r.kv_full0 = r.bar0 + 8 * kBKV;
+  r.kv_empty0 = r.kv_full0 + 8 * C::kSlots;
+  return r;
+}
+
+// ------------------------------------------------------------------ dQ ----
+template <int D>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdParams p) {
+  using C = BCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const BBars bb = init_bars<D>(sbase);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffBar + kBAbort);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + kBTmemSlot);
+  const Watchdog wd{p.wd.status, p.wd.limit_ns};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  int u = blockIdx.x;
+  const int qt = u % p.n_t;
+  u /= p.n_t;
+  const int r = u % p.P;
+  const int bh = u / p.P;
+  const int64_t C2 = p.L >> 1;
+  const int64_t q0 = static_cast<int64_t>(qt) * 128;
+  const int64_t nq = min64(128, p.L - q0);
+  const int64_t q_row0 = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(r) * p.L + q0;
+  const int64_t gq_max = p.causal ? zz_pos(r, q0 + nq - 1, C2, p.P) : 0;
+  auto make_iter = [&]() {
+    BIter it{0, 0, r, p.P, p.n_t, p.causal, -1, C2, gq_max, p.L};
+    it.settle();
+    return it;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bb.b(kBA), 1);
+    mbar_init(bb.b(kBS), 1);
+    mbar_init(bb.b(kBP), 128);
+    mbar_init(bb.b(kBO), 1);
+    mbar_init(bb.b(kBDrain), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bb.kv_full0 + 8 * s, 1);
+      mbar_init(bb.kv_empty0 + 8 * s, 1);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bb.b(kBA), 2 * C::kTile);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes, &tm_q, c * 64,
+                    static_cast<int32_t>(q_row0), bb.b(kBA));
+        tma_load_2d(sbase + C::kOffB + c * C::kChunkBytes, &tm_do, c * 64,
+                    static_cast<int32_t>(q_row0), bb.b(kBA));
+      }
+      int it = 0;
+      bool ok = true;
+      for (BIter ti = make_iter(); ok && ti.valid(); ++ti.t, ti.settle()) {
+        const int32_t ky = static_cast<int32_t>(static_cast<int64_t>(bh) * p.S +
+                                                static_cast<int64_t>(ti.blk) * p.L +
+                                                static_cast<int64_t>(ti.t) * 128);
+        for (int which = 0; which < 2 && ok; ++which, ++it) {
+          const int slot = it % C::kSlots;
+          if (!(ok = mbar_wait(bb.kv_empty0 + 8 * slot, ((it / C::kSlots) & 1) ^ 1, wd, abort_flag)))
+            break;
+          mbar_arrive_expect_tx(bb.kv_full0 + 8 * slot, C::kTile);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_2d(sbase + C::kOffKV + slot * C::kTile + c * C::kChunkBytes,
+                        which ? &tm_v : &tm_k, c * 64, ky, bb.kv_full0 + 8 * slot);
+        }
+      }
+      mbar_wait_drain(bb.b(kBA), 0, p.wd.limit_ns);
+      for (int i = max(0, it - C::kSlots); i < it; ++i)
+        mbar_wait_drain(bb.kv_full0 + 8 * (i % C::kSlots), (i / C::kSlots) & 1, p.wd.limit_ns);
+    }
+  } else if (warp == 1) {
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+    constexpr uint32_t kSlotDesc = C::kTile >> 4;
+    const uint64_t dQd = smem_desc_sw128(sbase + C::kOffA, 16, 1024);
+    const uint64_t dOd = smem_desc_sw128(sbase + C::kOffB, 16, 1024);
+    const uint64_t dKV = smem_desc_sw128(sbase + C::kOffKV, 16, 1024);
+    const uint64_t dKVmn = smem_desc_sw128(sbase + C::kOffKV, C::kChunkBytes, 1024);
+    bool issued = false;
+    BIter ti = make_iter();
+    if (ti.valid() && mbar_wait(bb.b(kBA), 0, wd, abort_flag)) {
+      tc_fence_after();
+      int it = 0;
+      for (int j = 0; ti.valid(); ++j, it += 2, ++ti.t, ti.settle()) {
+        const int ks = it % C::kSlots, vs = (it + 1) % C::kSlots;
+        if (!mbar_wait(bb.kv_full0 + 8 * ks, (it / C::kSlots) & 1, wd, abort_flag)) break;
+        if (!mbar_wait(bb.kv_full0 + 8 * vs, ((it + 1) / C::kSlots) & 1, wd, abort_flag)) break;
+        tc_fence_after();
+        issue_qk<D>(tmem + kColS, dQd, dKV + static_cast<uint64_t>(ks * kSlotDesc), idesc_s);
+        issue_qk<D>(tmem + kColP, dOd, dKV + static_cast<uint64_t>(vs * kSlotDesc), idesc_s);
+        mma_commit_e(bb.b(kBS));
+        mma_commit_e(bb.kv_empty0 + 8 * vs);
+        issued = true;
+        if (!mbar_wait(bb.b(kBP), j & 1, wd, abort_flag)) break;
+        tc_fence_after();
+        // dQ += dS K: dS over S's columns, K MN-major (d contiguous).
+        issue_pv(tmem + kColAcc0, tmem + kColS, dKVmn + static_cast<uint64_t>(ks * kSlotDesc),
+                 idesc_o, j > 0);
+        mma_commit_e(bb.kv_empty0 + 8 * ks);
+      }
+      if (!*abort_flag) mma_commit_e(bb.b(kBO));
+    }
+    if (issued) {
+      mma_commit_e(bb.b(kBDrain));
+      mbar_wait_drain(bb.b(kBDrain), 0, p.wd.limit_ns);
+    }
+  } else if (warp >= 4) {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_bits + kColS, tP = tmem + lane_bits + kColP;
+    const uint32_t tQ = tmem + lane_bits + kColAcc0;
+    const bool valid = row < nq;
+    const int64_t grow = q_row0 + row;
+    const float lse2 = valid ? p.lse[grow] * kLog2eB : 0.f;
+    const float Drow = valid ? p.Dv[grow] : 0.f;
+    const int64_t gq = p.causal ? zz_pos(r, min64(q0 + row, p.L - 1), C2, p.P) : 0;
+    const float sl2 = p.scale_log2;
+    int j = 0;
+    for (BIter ti = make_iter(); ti.valid(); ++j, ++ti.t, ti.settle()) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBS), j & 1, wd, abort_flag))) break;
+      tc_fence_after();
+      const int64_t k0 = static_cast<int64_t>(ti.t) * 128;
+      int nvis = static_cast<int>(min64(128, p.L - k0));
+      if (p.causal) nvis = causal_visible(ti.blk, k0, gq, p.L, p.P);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float sv[32], pv[32];
+        tmem_ld32(tS + c * 32, sv);
+        tmem_ld32(tP + c * 32, pv);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const int cc = c * 32 + 2 * x;
+          const float p0 = cc < nvis ? ex2(fmaf(sv[2 * x], sl2, -lse2)) : 0.f;
+          const float p1 = cc + 1 < nvis ? ex2(fmaf(sv[2 * x + 1], sl2, -lse2)) : 0.f;
+          pk[x] = pack_bf16x2(p0 * (pv[2 * x] - Drow), p1 * (pv[2 * x + 1] - Drow));
+        }
+        tmem_st16(tS + c * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bb.b(kBP));
+    }
+    __syncwarp();
+    const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
+    if (!aborted) {
+      const bool have = j > 0 && __all_sync(0xffffffffu, mbar_wait(bb.b(kBO), 0, wd, abort_flag));
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        if (have) {
+          tmem_ld32(tQ + c * 32, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = 0.f;
+        }
+        if (valid) store_row_bf16(p.dq + grow * D + c * 32, o, p.scale);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- dK/dV ----
+template <int D>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const BwdParams p) {
+  using C = BCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const BBars bb = init_bars<D>(sbase);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffBar + kBAbort);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + kBTmemSlot);
+  float *sm_ld = reinterpret_cast<float *>(smem + C::kOffLD);  // [2][LSE 128 | D 128]
+  const Watchdog wd{p.wd.status, p.wd.limit_ns};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  int u = blockIdx.x;
+  const int kt = u % p.n_t;
+  u /= p.n_t;
+  const int b = u % p.P;
+  const int bh = u / p.P;
+  const int64_t C2 = p.L >> 1;
+  const int64_t k0 = static_cast<int64_t>(kt) * 128;
+  const int64_t nk = min64(128, p.L - k0);
+  const int64_t k_row0 = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(b) * p.L + k0;
+  const int64_t gk_min = p.causal ? zz_pos(b, k0, C2, p.P) : 0;
+  auto make_iter = [&]() {
+    BIter it{0, 0, b, p.P, p.n_t, p.causal, +1, C2, gk_min, p.L};
+    it.settle();
+    return it;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bb.b(kBA), 1);
+    mbar_init(bb.b(kBS), 1);
+    mbar_init(bb.b(kBP), 128);
+    mbar_init(bb.b(kBO), 1);
+    mbar_init(bb.b(kBDrain), 1);
+    mbar_init(bb.b(kBLd), 128);
+    mbar_init(bb.b(kBLd + 1), 128);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bb.kv_full0 + 8 * s, 1);
+      mbar_init(bb.kv_empty0 + 8 * s, 1);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bb.b(kBA), 2 * C::kTile);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes, &tm_k, c * 64,
+                    static_cast<int32_t>(k_row0), bb.b(kBA));
+        tma_load_2d(sbase + C::kOffB + c * C::kChunkBytes, &tm_v, c * 64,
+                    static_cast<int32_t>(k_row0), bb.b(kBA));
+      }
+      int it = 0;
+      bool ok = true;
+      for (BIter ti = make_iter(); ok && ti.valid(); ++ti.t, ti.settle()) {
+        const int32_t qy = static_cast<int32_t>(static_cast<int64_t>(bh) * p.S +
+                                                static_cast<int64_t>(ti.blk) * p.L +
+                                                static_cast<int64_t>(ti.t) * 128);
+        for (int which = 0; which < 2 && ok; ++which, ++it) {
+          const int slot = it % C::kSlots;
+          if (!(ok = mbar_wait(bb.kv_empty0 + 8 * slot, ((it / C::kSlots) & 1) ^ 1, wd, abort_flag)))
+            break;
+          mbar_arrive_expect_tx(bb.kv_full0 + 8 * slot, C::kTile);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_2d(sbase + C::kOffKV + slot * C::kTile + c * C::kChunkBytes,
+                        which ? &tm_do : &tm_q, c * 64, qy, bb.kv_full0 + 8 * slot);
+        }
+      }
+      mbar_wait_drain(bb.b(kBA), 0, p.wd.limit_ns);
+      for (int i = max(0, it - C::kSlots); i < it; ++i)
+        mbar_wait_drain(bb.kv_full0 + 8 * (i % C::kSlots), (i / C::kSlots) & 1, p.wd.limit_ns);
+    }
+  } else if (warp == 1) {
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+    constexpr uint32_t kSlotDesc = C::kTile >> 4;
+    const uint64_t dKd = smem_desc_sw128(sbase + C::kOffA, 16, 1024);
+    const uint64_t dVd = smem_desc_sw128(sbase + C::kOffB, 16, 1024);
+    const uint64_t dRing = smem_desc_sw128(sbase + C::kOffKV, 16, 1024);
+    const uint64_t dRingMn = smem_desc_sw128(sbase + C::kOffKV, C::kChunkBytes, 1024);
+    bool issued = false;
+    BIter ti = make_iter();
+    if (ti.valid() && mbar_wait(bb.b(kBA), 0, wd, abort_flag)) {
+      tc_fence_after();
+      int it = 0;
+      for (int j = 0; ti.valid(); ++j, it += 2, ++ti.t, ti.settle()) {
+        const int qs = it % C::kSlots, gs = (it + 1) % C::kSlots;
+        if (!mbar_wait(bb.kv_full0 + 8 * qs, (it / C::kSlots) & 1, wd, abort_flag)) break;
+        if (!mbar_wait(bb.kv_full0 + 8 * gs, ((it + 1) / C::kSlots) & 1, wd, abort_flag)) break;
+        tc_fence_after();
+        // S^T = K Q^T and dP^T = V dO^T (rows = keys, columns = queries).
+        issue_qk<D>(tmem + kColS, dKd, dRing + static_cast<uint64_t>(qs * kSlotDesc), idesc_s);
+        issue_qk<D>(tmem + kColP, dVd, dRing + static_cast<uint64_t>(gs * kSlotDesc), idesc_s);
+        mma_commit_e(bb.b(kBS));
+        issued = true;
+        if (!mbar_wait(bb.b(kBP), j & 1, wd, abort_flag)) break;
+        tc_fence_after();
+        // dV += P^T dO and dK += dS^T Q (dO, Q MN-major).
+        issue_pv(tmem + kColAcc0, tmem + kColS, dRingMn + static_cast<uint64_t>(gs * kSlotDesc),
+                 idesc_o, j > 0);
+        issue_pv(tmem + kColAcc1, tmem + kColP, dRingMn + static_cast<uint64_t>(qs * kSlotDesc),
+                 idesc_o, j > 0);
+        mma_commit_e(bb.kv_empty0 + 8 * qs);
+        mma_commit_e(bb.kv_empty0 + 8 * gs);
+      }
+      if (!*abort_flag) mma_commit_e(bb.b(kBO));
+    }
+    if (issued) {
+      mma_commit_e(bb.b(kBDrain));
+      mbar_wait_drain(bb.b(kBDrain), 0, p.wd.limit_ns);
+    }
+  } else if (warp >= 4) {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // key row of the tile
+    const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_bits + kColS, tP = tmem + lane_bits + kColP;
+    const uint32_t tV = tmem + lane_bits + kColAcc0, tK = tmem + lane_bits + kColAcc1;
+    const bool kvalid = row < nk;
+    const int64_t gk = p.causal ? zz_pos(b, min64(k0 + row, p.L - 1), C2, p.P) : 0;
+    const float sl2 = p.scale_log2;
+    int j = 0;
+    for (BIter ti = make_iter(); ti.valid(); ++j, ++ti.t, ti.settle()) {
+      // This query tile's LSE (log2 units) and D, double-buffered in SMEM.
+      float *ld = sm_ld + (j & 1) * 256;
+      const int64_t q0 = static_cast<int64_t>(ti.t) * 128;
+      const int64_t nq = min64(128, p.L - q0);
+      const int64_t qrow = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(ti.blk) * p.L + q0 + row;
+      // Buffer j&1 was last read two tiles ago; no thread can still be there,
+      // since this tile's S needs every thread's arrival for the previous one.
+      ld[row] = row < nq ? p.lse[qrow] * kLog2eB : 0.f;
+      ld[128 + row] = row < nq ? p.Dv[qrow] : 0.f;
+      mbar_arrive(bb.b(kBLd + (j & 1)));  // release: the values above
+      if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBLd + (j & 1)), (j >> 1) & 1, wd, abort_flag)))
+        break;
+      // Visible queries of this key: positions >= its own (a suffix of the tile).
+      int first = 0, last = static_cast<int>(nq);
+      if (!kvalid) first = last;
+      else if (p.causal) first = causal_visible(ti.blk, q0, gk - 1, p.L, p.P);
+      if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBS), j & 1, wd, abort_flag))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float sv[32], pv[32];
+        tmem_ld32(tS + c * 32, sv);
+        tmem_ld32(tP + c * 32, pv);
+        tmem_wait_ld();
+        uint32_t pkp[16], pks[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const int cc = c * 32 + 2 * x;
+          const bool v0 = cc >= first && cc < last, v1 = cc + 1 >= first && cc + 1 < last;
+          const float p0 = v0 ? ex2(fmaf(sv[2 * x], sl2, -ld[cc])) : 0.f;
+          const float p1 = v1 ? ex2(fmaf(sv[2 * x + 1], sl2, -ld[cc + 1])) : 0.f;
+          pkp[x] = pack_bf16x2(p0, p1);
+          pks[x] = pack_bf16x2(p0 * (pv[2 * x] - ld[128 + cc]), p1 * (pv[2 * x + 1] - ld[128 + cc + 1]));
+        }
+        tmem_st16(tS + c * 16, pkp);
+        tmem_st16(tP + c * 16, pks);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bb.b(kBP));
+    }
+    __syncwarp();
+    const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
+    if (!aborted) {
+      const bool have = j > 0 && __all_sync(0xffffffffu, mbar_wait(bb.b(kBO), 0, wd, abort_flag));
+      tc_fence_after();
+      const int64_t grow = k_row0 + row;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        if (have) {
+          tmem_ld32(tV + c * 32, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = 0.f;
+        }
+        if (kvalid) store_row_bf16(p.dv + grow * D + c * 32, o, 1.f);
+      }
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        if (have) {
+          tmem_ld32(tK + c * 32, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = 0.f;
+        }
+        if (kvalid) store_row_bf16(p.dk + grow * D + c * 32, o, p.scale);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host ----
+typedef CUresult (*EncodeTiledFnB)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFnB encode_fn_b() {
+  static EncodeTiledFnB fn = [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<EncodeTiledFnB>(ptr);
+  }();
+  return fn;
+}
+
+cudaError_t row_map_b(CUtensorMap *map, const void *base, int64_t rows, int d) {
+  EncodeTiledFnB fn = encode_fn_b();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D>
+cudaError_t launch_bwd_variant(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                               const CUtensorMap &mdo, const BwdParams &p, int64_t units,
+                               cudaStream_t stream) {
+  using C = BCfg<D>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  C::kSmemBytes)) != cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(bwd_dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  C::kSmemBytes)) != cudaSuccess)
+      return e;
+    configured[dev] = true;
+  }
+  bwd_dq_kernel<D><<<static_cast<unsigned>(units), kThreadsB, C::kSmemBytes, stream>>>(mq, mk, mv,
+                                                                                       mdo, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_dkv_kernel<D><<<static_cast<unsigned>(units), kThreadsB, C::kSmemBytes, stream>>>(mq, mk, mv,
+                                                                                        mdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd(const void *q, const void *k, const void *v, const void *out,
+                            const void *dout, int d, const BwdParams &p, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(p.BH) * p.S;
+  if (rows == 0) return cudaSuccess;
+  const int64_t units = static_cast<int64_t>(p.BH) * p.P * p.n_t;
+  if (units > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  const int64_t prep_blocks = (rows + 7) / 8;
+  bwd_prep_kernel<<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16 *>(out), static_cast<const __nv_bfloat16 *>(dout), p.Dv, rows,
+      d);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mq, mk, mv, mdo;
+  if ((e = row_map_b(&mq, q, rows, d)) != cudaSuccess) return e;
+  if ((e = row_map_b(&mk, k, rows, d)) != cudaSuccess) return e;
+  if ((e = row_map_b(&mv, v, rows, d)) != cudaSuccess) return e;
+  if ((e = row_map_b(&mdo, dout, rows, d)) != cudaSuccess) return e;
+  return d == 128 ? launch_bwd_variant<128>(mq, mk, mv, mdo, p, units, stream)
+                  : launch_bwd_variant<64>(mq, mk, mv, mdo, p, units, stream);
+}
+
+}  // namespace ra

@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -44,6 +45,21 @@ struct AttnParams {
   int64_t kv_rank_stride;
   WatchdogParams wd;
 };
+
+// Backward pass (attn_bwd.cu).  All tensors [BH, S, d] in sharded order.
+struct BwdParams {
+  int BH, P, n_t;  // n_t = ceil(L / 128) tiles per rank chunk / ring block
+  int64_t S, L;
+  int causal;
+  float scale_log2, scale;
+  const float *lse;  // forward LSE [BH, S]
+  float *Dv;         // D_i = dO_i . O_i [BH, S] (scratch, written by the prep kernel)
+  __nv_bfloat16 *dq, *dk, *dv;
+  WatchdogParams wd;
+};
+
+cudaError_t launch_attn_bwd(const void *q, const void *k, const void *v, const void *out,
+                            const void *dout, int d, const BwdParams &p, cudaStream_t stream);
 
 // Launches the attention kernel.  q/k/v: bf16 row matrices [rows, d].
 cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k, const void *v,
