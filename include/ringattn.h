@@ -144,6 +144,55 @@ int ring_attn_bwd(const void *q, const void *k, const void *v, const void *out, 
 /* Workspace bytes of ring_attn_bwd (0 on bad arguments). */
 size_t ring_attn_bwd_workspace(int B, int H, int64_t S);
 
+/* Ulysses all-to-all (k8ai "Sequence and Context Parallel", "An alternative:
+ * all-to-all on heads": switch from split-by-sequence to split-by-heads
+ * around attention, then back).  Row permutation of a bf16 tensor of
+ * B*H*S rows of d elements between two per-rank layouts (P divides H):
+ *   sequence-split  [P][B][H][L][d]    rank r holds its L = S/P tokens of every head;
+ *   head-split      [P][B][H/P][S][d]  rank r holds heads r*H/P .. of every token
+ *                                      (token r*L + i = row i of rank r).
+ * inverse = 0: sequence-split -> head-split; 1: back.  Bit-exact copy. */
+int ra_ulysses_a2a(const void *x, void *y, int B, int H, int64_t S, int d, int P, int inverse,
+                   void *stream);
+
+/* Attention with Ulysses parallelism: q, k, v, out bf16 and lse fp32 in the
+ * sequence-split per-rank layout above ([P][B][H][L][d] / [P][B][H][L]);
+ * all-to-all to head-split, full attention of every token over all S keys
+ * for each rank's H/P heads (causal: key <= query by token position, S even),
+ * all-to-all back.  Equals full attention.  Requires H % P == 0 (the degree is
+ * at most the number of heads).  workspace: >= ulysses_attn_workspace(...)
+ * bytes, 256-byte aligned, used by this call only. */
+int ulysses_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                     int H, int64_t S, int d, int P, int causal, void *workspace, size_t ws_bytes,
+                     void *stream);
+
+/* Workspace bytes of ulysses_attn_fwd (0 on bad arguments). */
+size_t ulysses_attn_workspace(int B, int H, int64_t S, int d);
+
+/* The all-gather and reduce-scatter forms of context parallelism ("the NVIDIA
+ * context parallel package describes all-gather, reduce-scatter, and
+ * ring-based communication options", ultralytics glossary, "How Context
+ * Parallelism Works").  q, k, v, out: bf16 per-rank buffers [P][B][H][L][d]
+ * (rank r's L = S/P tokens of every head, in the order ra_cp_shard gives its
+ * chunk: contiguous, or zigzag when causal); lse: fp32 [P][B][H][L].  Both
+ * equal full attention.
+ *  cp_allgather_attn_fwd:     K and V are all-gathered into one rank-major
+ *                             copy, then every rank attends its queries to all
+ *                             S keys (blocks in ring order, one accumulator).
+ *  cp_reducescatter_attn_fwd: queries are all-gathered; each rank's K/V block
+ *                             yields a partial (O, LSE) for every query; the
+ *                             partials of each query are merged (the reduce)
+ *                             and each rank's rows are scattered back.
+ * workspace: >= cp_variant_workspace(...) bytes (either form), 256-byte
+ * aligned, used by this call only. */
+int cp_allgather_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                          int B, int H, int64_t S, int d, int P, int causal, void *workspace,
+                          size_t ws_bytes, void *stream);
+int cp_reducescatter_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                              int B, int H, int64_t S, int d, int P, int causal, void *workspace,
+                              size_t ws_bytes, void *stream);
+size_t cp_variant_workspace(int B, int H, int64_t S, int d, int P);
+
 /* Online-softmax merge of n normalised partials of the same rows ("the online
  * softmax trick", "day 83" blog, "Context parallelism: splitting the
  * sequence"):  M = max_i LSE_i,  w_i = exp(LSE_i - M),

@@ -8,6 +8,9 @@ from . import accounting  # noqa: F401
 from ._abi import (  # noqa: F401
     EXPORTS,
     RingAttnError,
+    cp_allgather_attn_fwd,
+    cp_reducescatter_attn_fwd,
+    cp_variant_workspace,
     factored_attn,
     factored_attn_static,
     factored_attn_workspace,
@@ -19,6 +22,7 @@ from ._abi import (  # noqa: F401
     ra_get_status,
     ra_ring_source,
     ra_set_watchdog_ns,
+    ra_ulysses_a2a,
     ra_watchdog_selftest,
     ring_attn_fwd,
     ring_attn_bwd,
@@ -26,4 +30,6 @@ from ._abi import (  # noqa: F401
     ring_attn_fwd_overlap,
     ring_attn_fwd_overlap_workspace,
     ring_attn_fwd_rank,
+    ulysses_attn_fwd,
+    ulysses_attn_workspace,
 )

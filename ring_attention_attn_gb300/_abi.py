@@ -25,6 +25,8 @@ ERRORS = {-1: "RA_ERR_ARG", -2: "RA_ERR_SHAPE", -3: "RA_ERR_ALIGN", -4: "RA_ERR_
 EXPORTS = ("ra_cp_shard_index", "ra_ring_source", "ra_cp_shard", "ra_frame_transpose",
            "ring_attn_fwd", "ring_attn_fwd_rank", "ring_attn_fwd_overlap",
            "ring_attn_fwd_overlap_workspace", "ring_attn_bwd", "ring_attn_bwd_workspace",
+           "ra_ulysses_a2a", "ulysses_attn_fwd", "ulysses_attn_workspace",
+           "cp_allgather_attn_fwd", "cp_reducescatter_attn_fwd", "cp_variant_workspace",
            "lse_merge", "factored_attn",
            "factored_attn_workspace", "factored_attn_static", "ra_get_status",
            "ra_set_watchdog_ns",
@@ -68,6 +70,15 @@ def lib():
                 "ring_attn_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32, i32,
                                         i32, vp, sz, vp]),
                 "ring_attn_bwd_workspace": (sz, [i32, i32, i64]),
+                "ra_ulysses_a2a": (i32, [vp, vp, i32, i32, i64, i32, i32, i32, vp]),
+                "ulysses_attn_fwd": (i32, [vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32, vp, sz,
+                                           vp]),
+                "ulysses_attn_workspace": (sz, [i32, i32, i64, i32]),
+                "cp_allgather_attn_fwd": (i32, [vp, vp, vp, vp, vp, i32, i32, i64, i32, i32, i32,
+                                                vp, sz, vp]),
+                "cp_reducescatter_attn_fwd": (i32, [vp, vp, vp, vp, vp, i32, i32, i64, i32, i32,
+                                                    i32, vp, sz, vp]),
+                "cp_variant_workspace": (sz, [i32, i32, i64, i32, i32]),
                 "lse_merge": (i32, [vp, vp, i32, i64, i32, vp, vp, vp]),
                 "factored_attn": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                         vp, sz, vp]),
@@ -238,6 +249,74 @@ def ring_attn_bwd(q, k, v, out, lse, dout, P: int, causal: bool = False, workspa
                                _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
                                _stream(stream)), "ring_attn_bwd")
     return dq, dk, dv
+
+
+def ra_ulysses_a2a(x, B: int, H: int, S: int, P: int, inverse: bool = False, out=None,
+                   stream=None):
+    """Ulysses all-to-all: sequence-split [P,B,H,S/P,d] <-> head-split [P,B,H/P,S,d]."""
+    import torch
+    d = x.shape[-1]
+    shape = (P, B, H, S // P, d) if inverse else (P, B, H // P, S, d)
+    y = torch.empty(shape, dtype=x.dtype, device=x.device) if out is None else out
+    _check(lib().ra_ulysses_a2a(_dev(x, torch.bfloat16, "x"), _dev(y, torch.bfloat16, "out"), B, H,
+                                S, d, P, int(inverse), _stream(stream)), "ra_ulysses_a2a")
+    return y
+
+
+def ulysses_attn_workspace(B: int, H: int, S: int, d: int) -> int:
+    return int(lib().ulysses_attn_workspace(B, H, S, d))
+
+
+def ulysses_attn_fwd(q, k, v, B: int, H: int, S: int, P: int, causal: bool = False,
+                     workspace=None, out=None, lse=None, stream=None):
+    """Attention with Ulysses parallelism; q/k/v sequence-split [P,B,H,S/P,d] bf16.
+    Returns out (same layout) and lse [P,B,H,S/P]."""
+    import torch
+    d = q.shape[-1]
+    need = ulysses_attn_workspace(B, H, S, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib().ulysses_attn_fwd(_dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"),
+                                  _dev(v, torch.bfloat16, "v"), _dev(out, torch.bfloat16, "out"),
+                                  _dev(lse, torch.float32, "lse"), B, H, S, d, P, int(causal),
+                                  _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                  _stream(stream)), "ulysses_attn_fwd")
+    return out, lse
+
+
+def cp_variant_workspace(B: int, H: int, S: int, d: int, P: int) -> int:
+    return int(lib().cp_variant_workspace(B, H, S, d, P))
+
+
+def _cp_variant(fn, name, q, k, v, B, H, S, P, causal, workspace, out, lse, stream):
+    import torch
+    d = q.shape[-1]
+    need = cp_variant_workspace(B, H, S, d, P)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(fn(_dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"),
+              _dev(v, torch.bfloat16, "v"), _dev(out, torch.bfloat16, "out"),
+              _dev(lse, torch.float32, "lse"), B, H, S, d, P, int(causal),
+              _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)), name)
+    return out, lse
+
+
+def cp_allgather_attn_fwd(q, k, v, B: int, H: int, S: int, P: int, causal: bool = False,
+                          workspace=None, out=None, lse=None, stream=None):
+    """All-gather form: per-rank buffers [P,B,H,S/P,d]; K/V gathered, then local attention."""
+    return _cp_variant(lib().cp_allgather_attn_fwd, "cp_allgather_attn_fwd", q, k, v, B, H, S, P,
+                       causal, workspace, out, lse, stream)
+
+
+def cp_reducescatter_attn_fwd(q, k, v, B: int, H: int, S: int, P: int, causal: bool = False,
+                              workspace=None, out=None, lse=None, stream=None):
+    """Reduce-scatter form: per-rank buffers; per-block partials merged per query."""
+    return _cp_variant(lib().cp_reducescatter_attn_fwd, "cp_reducescatter_attn_fwd", q, k, v, B,
+                       H, S, P, causal, workspace, out, lse, stream)
 
 
 def lse_merge(o_parts, lse_parts, out=None, lse_out=None, stream=None):

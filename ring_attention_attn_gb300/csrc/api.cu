@@ -333,6 +333,197 @@ int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
 
+int ra_ulysses_a2a(const void *x, void *y, int B, int H, int64_t S, int d, int P, int inverse,
+                   void *stream) {
+  if (B < 0 || H < 0 || S < 0 || P <= 0 || (inverse != 0 && inverse != 1)) return RA_ERR_ARG;
+  if (check_d(d) != RA_OK || S % P != 0 || H % P != 0) return RA_ERR_SHAPE;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH == 0 || S == 0) return RA_OK;
+  if (!x || !y) return RA_ERR_ARG;
+  if (!aligned16(x) || !aligned16(y)) return RA_ERR_ALIGN;
+  if (BH * S > kMaxRows) return RA_ERR_SHAPE;
+  cudaError_t e = ra::launch_row_permute(x, y, BH, S, d * 2, inverse ? 5 : 4, P, H, B,
+                                         as_stream(stream));
+  return e == cudaSuccess ? RA_OK : fail_cuda(e);
+}
+
+size_t ulysses_attn_workspace(int B, int H, int64_t S, int d) {
+  if (B < 0 || H < 0 || S < 0 || check_d(d) != RA_OK) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * S;
+  return 4 * ovl_part(rows * d * 2) + ovl_part(rows * 4);
+}
+
+int ulysses_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                     int H, int64_t S, int d, int P, int causal, void *workspace, size_t ws_bytes,
+                     void *stream) {
+  if (B < 0 || H < 0 || S < 0 || P <= 0 || (causal != 0 && causal != 1)) return RA_ERR_ARG;
+  if (check_d(d) != RA_OK || S % P != 0 || H % P != 0) return RA_ERR_SHAPE;
+  if (causal && S % 2 != 0) return RA_ERR_SHAPE;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH == 0 || S == 0) return RA_OK;
+  if (!q || !k || !v || !out || !lse) return RA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return RA_ERR_ALIGN;
+  if (BH * S > kMaxRows || BH > 0x7fffffff) return RA_ERR_SHAPE;
+  if (!workspace || ws_bytes < ulysses_attn_workspace(B, H, S, d)) return RA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RA_ERR_ALIGN;
+  cudaStream_t st = as_stream(stream);
+  ra::WatchdogParams wd;
+  if (!watchdog(&wd)) return fail_cuda(cudaGetLastError());
+  const size_t tb = ovl_part(static_cast<size_t>(BH * S) * d * 2);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  void *qh = ws, *kh = ws + tb, *vh = ws + 2 * tb, *oh = ws + 3 * tb;
+  float *lh = reinterpret_cast<float *>(ws + 4 * tb);
+  const void *src[3] = {q, k, v};
+  void *dst[3] = {qh, kh, vh};
+  cudaError_t e;
+  for (int i = 0; i < 3; ++i) {
+    e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 4, P, H, B, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  // Head-split: B*H heads of S tokens in global order; no ring (P = 1).
+  ra::AttnParams p{};
+  p.BH = static_cast<int>(BH);
+  p.G = 1;
+  p.n_ranks = 1;
+  p.n_stepgroups = 1;
+  p.n_pairs = static_cast<int>((S + 255) / 256);
+  p.q_rows_bh = S;
+  p.kv_rows_bh = S;
+  p.L = S;
+  p.P = 1;
+  p.steps_per_group = 1;
+  p.causal = causal;  // zigzag with one rank is the identity order
+  p.scale_log2 = scale_log2(d);
+  p.out = oh;
+  p.lse = lh;
+  p.wd = wd;
+  e = ra::launch_ring_attn(qh, BH * S, kh, vh, BH * S, d, false, p, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = ra::launch_row_permute(oh, out, BH, S, d * 2, 5, P, H, B, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  e = ra::launch_row_permute(lh, lse, BH, S, 4, 5, P, H, B, st);
+  return e == cudaSuccess ? RA_OK : fail_cuda(e);
+}
+
+// Workspace of the all-gather / reduce-scatter forms: three rank-major bf16
+// copies (Q, K, V), then fp32 partials [P][BH][S][d] + LSEs, then a rank-major
+// bf16 output and fp32 LSE.
+size_t cp_variant_workspace(int B, int H, int64_t S, int d, int P) {
+  if (B < 0 || H < 0 || S < 0 || P <= 0 || check_d(d) != RA_OK) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * S;
+  return 4 * ovl_part(rows * d * 2) + ovl_part(static_cast<size_t>(P) * rows * d * 4) +
+         ovl_part(static_cast<size_t>(P) * rows * 4) + ovl_part(rows * 4);
+}
+
+static int cp_variant_check(const void *q, const void *k, const void *v, void *out, float *lse,
+                            int B, int H, int64_t S, int d, int P, int causal, void *workspace,
+                            size_t ws_bytes) {
+  if (B < 0 || H < 0 || S < 0 || P <= 0 || P > 64 || (causal != 0 && causal != 1))
+    return RA_ERR_ARG;
+  if (check_d(d) != RA_OK || S % P != 0) return RA_ERR_SHAPE;
+  if (causal && S % (2 * static_cast<int64_t>(P)) != 0) return RA_ERR_SHAPE;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH == 0 || S == 0) return 1;  // no-op
+  if (!q || !k || !v || !out || !lse) return RA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return RA_ERR_ALIGN;
+  if (BH * S > kMaxRows || BH > 0x7fffffff) return RA_ERR_SHAPE;
+  if (!workspace || ws_bytes < cp_variant_workspace(B, H, S, d, P)) return RA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RA_ERR_ALIGN;
+  return RA_OK;
+}
+
+int cp_allgather_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                          int B, int H, int64_t S, int d, int P, int causal, void *workspace,
+                          size_t ws_bytes, void *stream) {
+  int rc = cp_variant_check(q, k, v, out, lse, B, H, S, d, P, causal, workspace, ws_bytes);
+  if (rc != RA_OK) return rc == 1 ? RA_OK : rc;
+  const int64_t BH = static_cast<int64_t>(B) * H, L = S / P;
+  cudaStream_t st = as_stream(stream);
+  ra::WatchdogParams wd;
+  if (!watchdog(&wd)) return fail_cuda(cudaGetLastError());
+  const size_t tb = ovl_part(static_cast<size_t>(BH * S) * d * 2);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  void *kg = ws + tb, *vg = ws + 2 * tb;
+  cudaError_t e = ra::launch_row_permute(k, kg, BH, S, d * 2, 6, P, H, B, st);
+  if (e == cudaSuccess) e = ra::launch_row_permute(v, vg, BH, S, d * 2, 6, P, H, B, st);
+  for (int r = 0; r < P && e == cudaSuccess; ++r) {
+    // Rank r: its own queries (buffer r) against every block of the gathered K/V.
+    ra::AttnParams p{};
+    p.BH = static_cast<int>(BH);
+    p.G = 1;
+    p.n_ranks = 1;
+    p.n_stepgroups = 1;
+    p.n_pairs = static_cast<int>((L + 255) / 256);
+    p.q_rows_bh = L;
+    p.kv_rows_bh = S;
+    p.L = L;
+    p.P = P;
+    p.rank_begin = r;
+    p.steps_per_group = P;
+    p.causal = causal;
+    p.scale_log2 = scale_log2(d);
+    p.out = static_cast<uint8_t *>(out) + static_cast<size_t>(r) * BH * L * d * 2;
+    p.lse = lse + static_cast<size_t>(r) * BH * L;
+    p.wd = wd;
+    const void *qr = static_cast<const uint8_t *>(q) + static_cast<size_t>(r) * BH * L * d * 2;
+    e = ra::launch_ring_attn(qr, BH * L, kg, vg, BH * S, d, false, p, st);
+  }
+  return e == cudaSuccess ? RA_OK : fail_cuda(e);
+}
+
+int cp_reducescatter_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                              int B, int H, int64_t S, int d, int P, int causal, void *workspace,
+                              size_t ws_bytes, void *stream) {
+  int rc = cp_variant_check(q, k, v, out, lse, B, H, S, d, P, causal, workspace, ws_bytes);
+  if (rc != RA_OK) return rc == 1 ? RA_OK : rc;
+  const int64_t BH = static_cast<int64_t>(B) * H, L = S / P;
+  cudaStream_t st = as_stream(stream);
+  ra::WatchdogParams wd;
+  if (!watchdog(&wd)) return fail_cuda(cudaGetLastError());
+  const size_t tb = ovl_part(static_cast<size_t>(BH * S) * d * 2);
+  const size_t pb = ovl_part(static_cast<size_t>(P) * BH * S * d * 4);
+  const size_t lb = ovl_part(static_cast<size_t>(P) * BH * S * 4);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  void *qg = ws, *kg = ws + tb, *vg = ws + 2 * tb, *og = ws + 3 * tb;
+  float *o_parts = reinterpret_cast<float *>(ws + 4 * tb);
+  float *l_parts = reinterpret_cast<float *>(ws + 4 * tb + pb);
+  float *lg = reinterpret_cast<float *>(ws + 4 * tb + pb + lb);
+  const void *src[3] = {q, k, v};
+  void *dst[3] = {qg, kg, vg};
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+    e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 6, P, H, B, st);
+  if (e == cudaSuccess) {
+    // Every (rank, block) pair once; the partial is filed under the block.
+    ra::AttnParams p{};
+    p.BH = static_cast<int>(BH);
+    p.G = 1;
+    p.n_ranks = P;
+    p.n_stepgroups = P;
+    p.n_pairs = static_cast<int>((L + 255) / 256);
+    p.q_rows_bh = S;
+    p.kv_rows_bh = S;
+    p.L = L;
+    p.P = P;
+    p.steps_per_group = 1;
+    p.causal = causal;
+    p.part_by_block = 1;
+    p.scale_log2 = scale_log2(d);
+    p.out = o_parts;
+    p.lse = l_parts;
+    p.out_part_stride = BH * S * d;
+    p.lse_part_stride = BH * S;
+    p.wd = wd;
+    e = ra::launch_ring_attn(qg, BH * S, kg, vg, BH * S, d, true, p, st);
+  }
+  if (e == cudaSuccess) e = ra::launch_lse_merge(o_parts, l_parts, P, BH * S, d, og, lg, st);
+  if (e == cudaSuccess) e = ra::launch_row_permute(og, out, BH, S, d * 2, 7, P, H, B, st);
+  if (e == cudaSuccess) e = ra::launch_row_permute(lg, lse, BH, S, 4, 7, P, H, B, st);
+  return e == cudaSuccess ? RA_OK : fail_cuda(e);
+}
+
 size_t ring_attn_bwd_workspace(int B, int H, int64_t S) {
   if (B < 0 || H < 0 || S < 0) return 0;
   return ovl_part(static_cast<size_t>(B) * H * S * 4);

@@ -496,12 +496,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!aborted) {
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
         const float lse_val = (l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+        const int part = p.part_by_block ? ((w.rank - w.s_lo) % p.P + p.P) % p.P : w.part;
         const int64_t orow =
             p.pack ? (static_cast<int64_t>(w.bh) * p.pN + static_cast<int64_t>(w.g) * p.pack + pr) *
                              p.pT + static_cast<int64_t>(w.rank) * p.Lf + (qi - static_cast<int64_t>(pr) * p.Lf)
                    : w.q_row0 + qi;
         if (OUT_F32) {
-          float *out = reinterpret_cast<float *>(p.out) + w.part * p.out_part_stride + orow * D;
+          float *out = reinterpret_cast<float *>(p.out) + part * p.out_part_stride + orow * D;
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
@@ -522,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           __nv_bfloat16 *out =
-              reinterpret_cast<__nv_bfloat16 *>(p.out) + w.part * p.out_part_stride + orow * D;
+              reinterpret_cast<__nv_bfloat16 *>(p.out) + part * p.out_part_stride + orow * D;
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
@@ -544,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (row_valid) p.lse[w.part * p.lse_part_stride + orow] = lse_val;
+        if (row_valid) p.lse[part * p.lse_part_stride + orow] = lse_val;
       }
     }
   }

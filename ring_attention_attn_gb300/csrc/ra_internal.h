@@ -43,6 +43,9 @@ struct AttnParams {
   // + L) of the K/V tensors, whatever block of the ring it holds.
   int kv_own;
   int64_t kv_rank_stride;
+  // Per-step partials indexed by the K/V block that produced them
+  // ((rank - step) mod P) instead of by step (reduce-scatter form).
+  int part_by_block;
   WatchdogParams wd;
 };
 

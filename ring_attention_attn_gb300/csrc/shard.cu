@@ -21,10 +21,43 @@ namespace {
 
 struct PermuteArgs {
   int64_t S;
-  int mode;       // 0 shard, 1 unshard, 2 [T,N]->[N,T], 3 [N,T]->[T,N]
-  int64_t a, b;   // modes 0/1: a = P; modes 2/3: a = T, b = N
-  int layout;     // modes 0/1: 0 contiguous, 1 zigzag
+  int mode;       // 0 shard, 1 unshard, 2 [T,N]->[N,T], 3 [N,T]->[T,N],
+                  // 4 Ulysses sequence-split -> head-split, 5 back,
+                  // 6 per-rank [P][B][H][L] -> rank-major [B][H][P*L], 7 back
+  int64_t a, b;   // modes 0/1: a = P; modes 2/3: a = T, b = N; modes 4-7: a = P, b = H
+  int layout;     // modes 0/1: 0 contiguous, 1 zigzag; modes 4-7: B
 };
+
+// Ulysses all-to-all (k8ai "An alternative: all-to-all on heads"), over the
+// whole tensor.  Sequence-split per-rank layout [P][B][H][L][d]: rank r's
+// chunk of every head.  Head-split per-rank layout [P][B][H/P][S][d]: rank
+// r's heads r*H/P .. (r+1)*H/P - 1, every token (contiguous split: token
+// r*L + i is row i of rank r).  Returns the source row of output row o.
+__device__ __forceinline__ int64_t ulysses_source_row(const PermuteArgs &p, int64_t o) {
+  const int64_t P = p.a, H = p.b, B = p.layout, S = p.S, L = S / P, Hp = H / P;
+  if (p.mode == 6) {  // output rank-major [B][H][S] <- input per-rank [P][B][H][L] (all-gather)
+    const int64_t bh = o / S, t = o - bh * S;
+    const int64_t r = t / L, i = t - r * L;
+    return (r * B * H + bh) * L + i;
+  }
+  if (p.mode == 7) {  // output per-rank <- input rank-major (scatter)
+    const int64_t r = o / (B * H * L), r1 = o - r * (B * H * L);
+    const int64_t bh = r1 / L, i = r1 - bh * L;
+    return bh * S + r * L + i;
+  }
+  if (p.mode == 4) {  // output head-split <- input sequence-split
+    const int64_t R = o / (B * Hp * S), r1 = o - R * (B * Hp * S);
+    const int64_t b = r1 / (Hp * S), r2 = r1 - b * (Hp * S);
+    const int64_t hh = r2 / S, t = r2 - hh * S;
+    const int64_t r = t / L, i = t - r * L;
+    return ((r * B + b) * H + R * Hp + hh) * L + i;
+  }
+  // output sequence-split <- input head-split
+  const int64_t r = o / (B * H * L), r1 = o - r * (B * H * L);
+  const int64_t b = r1 / (H * L), r2 = r1 - b * (H * L);
+  const int64_t h = r2 / L, i = r2 - h * L;
+  return (((h / Hp) * B + b) * Hp + (h % Hp)) * S + r * L + i;
+}
 
 // Source row (within one (b,h) slice) of output row o.
 __device__ __forceinline__ int64_t source_row(const PermuteArgs &p, int64_t o) {
@@ -72,8 +105,13 @@ __global__ void __launch_bounds__(256) row_permute_kernel(const Vec *__restrict_
       if (e < total) {
         const int64_t row = e / PIECES;
         const int piece = static_cast<int>(e - row * PIECES);
-        const int64_t bh = row / p.S, o = row - bh * p.S;
-        const int64_t src = bh * p.S + source_row(p, o);
+        int64_t src;
+        if (p.mode >= 4) {
+          src = ulysses_source_row(p, row);
+        } else {
+          const int64_t bh = row / p.S, o = row - bh * p.S;
+          src = bh * p.S + source_row(p, o);
+        }
         v[u] = x[src * PIECES + piece];
         dst[u] = e;
       }

@@ -235,6 +235,60 @@ def test_overlap_ring_matches_oracle_and_fused(B, H, S, d, P, causal, separate):
          ro, rl)
 
 
+# ----------------------------------------------------- Ulysses (all-to-all) --
+def _seq_split(x, P):
+    B, H, S, d = x.shape
+    return x.reshape(B, H, P, S // P, d).permute(2, 0, 1, 3, 4).contiguous()
+
+
+@pytest.mark.parametrize("B,H,S,d,P", [(1, 4, 512, 64, 2), (2, 8, 1200, 128, 4), (1, 2, 96, 128, 2)])
+def test_ulysses_all_to_all_bit_exact(B, H, S, d, P):
+    x, _, _ = synth.make_custom((B, H, S, d), (1, 1, 1, 1), seed=H * S)
+    xs = _seq_split(x, P)
+    y = ra.ra_ulysses_a2a(xs.cuda(), B, H, S, P)
+    L, Hp = S // P, H // P
+    ref = xs.reshape(P, B, P, Hp, L, d).permute(2, 1, 3, 0, 4, 5).reshape(P, B, Hp, S, d)
+    assert torch.equal(y.cpu().view(torch.int16), ref.view(torch.int16))
+    back = ra.ra_ulysses_a2a(y, B, H, S, P, inverse=True)
+    assert torch.equal(back.cpu().view(torch.int16), xs.view(torch.int16))
+
+
+@pytest.mark.parametrize("B,H,S,d,P,causal", [(1, 4, 1024, 64, 2, False), (1, 8, 1200, 128, 4, True),
+                                              (2, 4, 600, 128, 4, False)])
+def test_ulysses_attention_matches_oracle(B, H, S, d, P, causal):
+    q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=S + H + P)
+    o, l = ra.ulysses_attn_fwd(*(_seq_split(x, P).cuda() for x in (q, k, v)), B, H, S, P,
+                               causal=causal)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+    o = o.cpu().permute(1, 2, 0, 3, 4).reshape(B, H, S, d)
+    l = l.cpu().permute(1, 2, 0, 3).reshape(B, H, S)
+    ro, rl = oracle.attention(q, k, v, causal=causal)
+    _cmp(o, l, ro, rl)
+
+
+# ------------------------------------------ all-gather / reduce-scatter forms --
+def _per_rank(x, P, layout):
+    B, H, S, d = x.shape
+    return _shard_host(x, P, layout).reshape(B, H, P, S // P, d).permute(2, 0, 1, 3, 4).contiguous()
+
+
+@pytest.mark.parametrize("form", ["allgather", "reducescatter"])
+@pytest.mark.parametrize("B,H,S,d,P,causal", [(1, 2, 1024, 128, 4, False), (1, 2, 2048, 64, 2, True),
+                                              (2, 1, 600, 128, 3, True), (1, 3, 1000, 64, 8, False)])
+def test_allgather_reducescatter_forms_match_oracle(form, B, H, S, d, P, causal):
+    layout = 1 if causal else 0
+    q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=S + 5 * P + causal)
+    fn = ra.cp_allgather_attn_fwd if form == "allgather" else ra.cp_reducescatter_attn_fwd
+    o, l = fn(*(_per_rank(x, P, layout).cuda() for x in (q, k, v)), B, H, S, P, causal=causal)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+    o = _unshard_host(o.cpu().permute(1, 2, 0, 3, 4).reshape(B, H, S, d), P, layout)
+    l = _unshard_host(l.cpu().permute(1, 2, 0, 3).reshape(B, H, S, 1), P, layout).squeeze(-1)
+    ro, rl = oracle.attention(q, k, v, causal=causal)
+    _cmp(o, l, ro, rl)
+
+
 # ---------------------------------------------------------------- factored --
 def test_factored_small_full():
     B, H, T, N, d, P = 1, 2, 8, 50, 64, 4
