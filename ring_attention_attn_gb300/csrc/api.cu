@@ -109,6 +109,7 @@ int ra_cp_shard(const void *x, void *y, int64_t BH, int64_t S, int d, int P, int
   if (BH == 0 || S == 0) return RA_OK;
   if (!x || !y) return RA_ERR_ARG;
   if (!aligned16(x) || !aligned16(y)) return RA_ERR_ALIGN;
+  if (BH * S > kMaxRows) return RA_ERR_SHAPE;
   cudaError_t e = ra::launch_row_permute(x, y, BH, S, d * 2, inverse ? 1 : 0, P, 0, layout,
                                          as_stream(stream));
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
@@ -121,6 +122,7 @@ int ra_frame_transpose(const void *x, void *y, int64_t BH, int64_t T, int64_t N,
   if (BH == 0 || T == 0 || N == 0) return RA_OK;
   if (!x || !y) return RA_ERR_ARG;
   if (!aligned16(x) || !aligned16(y)) return RA_ERR_ALIGN;
+  if (BH * T * N > kMaxRows) return RA_ERR_SHAPE;
   cudaError_t e = ra::launch_row_permute(x, y, BH, T * N, d * 2, inverse ? 3 : 2, T, N, 0,
                                          as_stream(stream));
   return e == cudaSuccess ? RA_OK : fail_cuda(e);

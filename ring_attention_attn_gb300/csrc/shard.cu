@@ -32,31 +32,36 @@ struct PermuteArgs {
 // whole tensor.  Sequence-split per-rank layout [P][B][H][L][d]: rank r's
 // chunk of every head.  Head-split per-rank layout [P][B][H/P][S][d]: rank
 // r's heads r*H/P .. (r+1)*H/P - 1, every token (contiguous split: token
-// r*L + i is row i of rank r).  Returns the source row of output row o.
-__device__ __forceinline__ int64_t ulysses_source_row(const PermuteArgs &p, int64_t o) {
-  const int64_t P = p.a, H = p.b, B = p.layout, S = p.S, L = S / P, Hp = H / P;
-  if (p.mode == 6) {  // output rank-major [B][H][S] <- input per-rank [P][B][H][L] (all-gather)
-    const int64_t bh = o / S, t = o - bh * S;
-    const int64_t r = t / L, i = t - r * L;
+// r*L + i is row i of rank r).  Modes 6/7 gather per-rank buffers into the
+// rank-major order [B][H][P*L] and scatter back.  Returns the source row of
+// output row o.  Row counts are below 2^31, so 32-bit arithmetic is exact.
+__device__ __forceinline__ uint32_t global_source_row(const PermuteArgs &p, uint32_t o) {
+  const uint32_t P = static_cast<uint32_t>(p.a), H = static_cast<uint32_t>(p.b);
+  const uint32_t B = static_cast<uint32_t>(p.layout), S = static_cast<uint32_t>(p.S);
+  const uint32_t L = S / P, Hp = H / P;
+  if (p.mode == 6) {  // rank-major [B][H][S] <- per-rank [P][B][H][L] (all-gather)
+    const uint32_t bh = o / S, t = o - bh * S;
+    const uint32_t r = t / L, i = t - r * L;
     return (r * B * H + bh) * L + i;
   }
-  if (p.mode == 7) {  // output per-rank <- input rank-major (scatter)
-    const int64_t r = o / (B * H * L), r1 = o - r * (B * H * L);
-    const int64_t bh = r1 / L, i = r1 - bh * L;
+  if (p.mode == 7) {  // per-rank <- rank-major (scatter)
+    const uint32_t r = o / (B * H * L), r1 = o - r * (B * H * L);
+    const uint32_t bh = r1 / L, i = r1 - bh * L;
     return bh * S + r * L + i;
   }
-  if (p.mode == 4) {  // output head-split <- input sequence-split
-    const int64_t R = o / (B * Hp * S), r1 = o - R * (B * Hp * S);
-    const int64_t b = r1 / (Hp * S), r2 = r1 - b * (Hp * S);
-    const int64_t hh = r2 / S, t = r2 - hh * S;
-    const int64_t r = t / L, i = t - r * L;
+  if (p.mode == 4) {  // head-split <- sequence-split
+    const uint32_t R = o / (B * Hp * S), r1 = o - R * (B * Hp * S);
+    const uint32_t b = r1 / (Hp * S), r2 = r1 - b * (Hp * S);
+    const uint32_t hh = r2 / S, t = r2 - hh * S;
+    const uint32_t r = t / L, i = t - r * L;
     return ((r * B + b) * H + R * Hp + hh) * L + i;
   }
-  // output sequence-split <- input head-split
-  const int64_t r = o / (B * H * L), r1 = o - r * (B * H * L);
-  const int64_t b = r1 / (H * L), r2 = r1 - b * (H * L);
-  const int64_t h = r2 / L, i = r2 - h * L;
-  return (((h / Hp) * B + b) * Hp + (h % Hp)) * S + r * L + i;
+  // sequence-split <- head-split
+  const uint32_t r = o / (B * H * L), r1 = o - r * (B * H * L);
+  const uint32_t b = r1 / (H * L), r2 = r1 - b * (H * L);
+  const uint32_t h = r2 / L, i = r2 - h * L;
+  const uint32_t R = h / Hp;
+  return ((R * B + b) * Hp + (h - R * Hp)) * S + r * L + i;
 }
 
 // Source row (within one (b,h) slice) of output row o.
@@ -107,7 +112,7 @@ __global__ void __launch_bounds__(256) row_permute_kernel(const Vec *__restrict_
         const int piece = static_cast<int>(e - row * PIECES);
         int64_t src;
         if (p.mode >= 4) {
-          src = ulysses_source_row(p, row);
+          src = global_source_row(p, static_cast<uint32_t>(row));
         } else {
           const int64_t bh = row / p.S, o = row - bh * p.S;
           src = bh * p.S + source_row(p, o);

@@ -85,6 +85,20 @@ def test_argument_errors_are_reported_before_any_launch():
                            good, 16, s) == -6
 
 
+def test_sizes_beyond_the_addressable_rows_are_rejected():
+    """Row indices are 32-bit in the tensor maps and index math: B*H*S rows
+    must stay below 2^31 - 512; larger inputs fail on the host."""
+    L = _abi.lib()
+    vp = ctypes.c_void_p
+    good, s = vp(256), vp(0)
+    S = 1 << 27  # 2^27 tokens x 16 heads = 2^31 rows
+    assert L.ring_attn_fwd(good, good, good, good, good, 1, 16, S, 64, 1, 0, s) == -2
+    assert L.ring_attn_fwd_rank(good, good, good, good, good, 1, 16, S, 64, 8, 0, 0, 0, 8, 1, s) == -2
+    assert L.ra_cp_shard(good, good, 16, S, 64, 1, 0, 0, s) == -2
+    assert L.ra_frame_transpose(good, good, 16, 1 << 14, 1 << 13, 64, 0, s) == -2
+    assert L.ra_ulysses_a2a(good, good, 1, 16, S, 64, 2, 0, s) == -2
+
+
 def test_workspace_size():
     L = _abi.lib()
     rows = 1 * 24 * 48 * 900
