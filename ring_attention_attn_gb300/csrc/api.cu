@@ -667,6 +667,9 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
       p.pT = T;
       p.G = (N + pack - 1) / pack;
       p.L = static_cast<int64_t>(pack) * L;
+      // Two ranks' chunks per CTA (its two query tiles share the key tiles).
+      p.n_ranks = (P + 1) / 2;
+      p.pack_ranks = P;
       p.n_pairs = 1;
     }
     p.P = P;

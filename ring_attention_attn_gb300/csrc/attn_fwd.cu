@@ -11,8 +11,12 @@
 // and finally writes O / l and LSE = m + ln l.  Scores are q.k / sqrt(d),
 // masked by global token position (key <= query) for the zigzag causal split.
 //
-// CTA structure (384 threads, one CTA per SM, ~225 KB shared memory):
-//   warp 0       TMA producer: Q tile pair once, then K_j, V_j tiles through a
+// CTA structure (384 threads, one CTA per SM, ~225 KB shared memory).  A
+// unit is one query-tile pair with its steps; a CTA runs one unit, or, for
+// short units, walks units blockIdx.x + k * gridDim.x (persistent), every
+// role counting barrier phases across units:
+//   warp 0       TMA producer: per unit the Q tile pair (once the previous
+//                pair's last QK^T is done), then K_j, V_j tiles through a
 //                ring of shared-memory slots (mbarrier full/empty pairs).
 //   warp 1       allocates 512 TMEM columns and issues every tcgen05.mma and
 //                tcgen05.commit: the whole warp runs the issue loop (so its
@@ -47,6 +51,7 @@ constexpr int kThreads = 384;
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per tile
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kPersistMaxTiles = 32;  // key tiles per unit up to which CTAs persist
 constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D>
@@ -61,7 +66,7 @@ struct Cfg {
   static constexpr int kOffKV = 2 * kQTile;
   static constexpr int kOffBar = kOffKV + kSlots * kKVTile;
   static constexpr int kBarBytes = 512;
-  static_assert(8 * (8 + 2 * kSlots) <= 496, "barriers overlap the TMEM slot");
+  static_assert(8 * (9 + 2 * kSlots) <= 496, "barriers overlap the TMEM slot");
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
 };
 
@@ -72,7 +77,8 @@ enum : int {
   kBarPFull = 3,   // +wg
   kBarODone = 5,   // +wg
   kBarDrain = 7,
-  kBarKVFull = 8,  // +slot; kv_empty follows the kv_full block
+  kBarQEmpty = 8,  // the Q pair's last QK^T has completed
+  kBarKVFull = 9,  // +slot; kv_empty follows the kv_full block
 };
 constexpr int kTmemSlotOff = 496;
 constexpr int kAbortOff = 500;
@@ -111,7 +117,7 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams &p, int u) {
   u /= p.n_ranks;
   w.g = u % p.G;
   w.bh = u / p.G;
-  w.rank = p.rank_begin + ri;
+  w.rank = p.rank_begin + (p.pack_ranks ? 2 * ri : ri);
   w.s_lo = p.step_begin + w.part * p.steps_per_group;
   w.s_hi = w.s_lo + p.steps_per_group;
   w.q_row0 = static_cast<int64_t>(w.bh) * p.q_rows_bh + static_cast<int64_t>(w.g) * p.q_rows_g +
@@ -152,11 +158,31 @@ struct TileIter {
   __device__ __forceinline__ bool valid(const Unit &w) const { return s < w.s_hi; }
 };
 
+// Geometry of one unit: its query-tile pair, whether the second tile holds
+// rows, and (causal) the last global query position of the pair.
+struct UnitGeo {
+  Unit w;
+  int64_t pair_row0, gq_max;
+  bool has_q1;
+};
+
+__device__ __forceinline__ UnitGeo unit_geo(const AttnParams &p, int u) {
+  UnitGeo g;
+  g.w = decode_unit(p, u);
+  g.pair_row0 = static_cast<int64_t>(g.w.pair) * 2 * kBM;
+  // Packed mode pairs rank chunks: tile 1 is the next rank's chunk.
+  g.has_q1 = p.pack ? (p.pack_ranks > 0 && g.w.rank + 1 < p.rank_begin + p.pack_ranks)
+                    : g.pair_row0 + kBM < p.L;
+  g.gq_max = p.causal ? zz_pos(g.w.rank, min64(g.pair_row0 + 2 * kBM - 1, p.L - 1), p.L >> 1, p.P)
+                      : 0;
+  return g;
+}
+
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p, int n_units) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -171,16 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const Unit w = decode_unit(p, blockIdx.x);
   const int n_t = static_cast<int>((p.L + kBN - 1) / kBN);
-  const int64_t pair_row0 = static_cast<int64_t>(w.pair) * 2 * kBM;
-  const bool has_q1 = pair_row0 + kBM < p.L;
-  const int64_t half = p.L >> 1;
-  const int64_t gq_max =
-      p.causal ? zz_pos(w.rank, min64(pair_row0 + 2 * kBM - 1, p.L - 1), half, p.P) : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar0 + 8 * kBarQFull, 1);
+    mbar_init(bar0 + 8 * kBarQEmpty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar0 + 8 * (kBarSFull + i), 1);
       mbar_init(bar0 + 8 * (kBarPFull + i), 128);
@@ -195,17 +216,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_fence_init();
   }
   if (p.pack) {
-    // Rows past pack * Lf of the Q tile and of every K/V slot are never
+    // Rows past pack * Lf of the Q tiles and of every K/V slot are never
     // written by TMA: zero them once so that masked keys meet finite values
     // (P = 0 times V must stay 0).
     const int r0 = p.pack * p.Lf;
     const int per_chunk = (kBM - r0) * 8;  // 16-byte units
-    const int regions = (C::kSlots + 1) * C::kChunks;
+    const int regions = (C::kSlots + 2) * C::kChunks;
     for (int idx = threadIdx.x; idx < regions * per_chunk; idx += kThreads) {
       const int reg = idx / per_chunk, u = idx - reg * per_chunk;
       const int slot = reg / C::kChunks, c = reg - slot * C::kChunks;
-      const uint32_t base = (slot < C::kSlots ? sbase + C::kOffKV + slot * C::kKVTile
-                                              : sbase + C::kOffQ0) + c * C::kChunkBytes;
+      const uint32_t base = (slot < C::kSlots    ? sbase + C::kOffKV + slot * C::kKVTile
+                             : slot == C::kSlots ? sbase + C::kOffQ0
+                                                 : sbase + C::kOffQ1) +
+                            c * C::kChunkBytes;
       st_shared_v4(base + r0 * 128 + u * 16, 0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
@@ -221,76 +244,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Every role walks the same units (blockIdx.x, + gridDim.x, ...) and skips
+  // the same empty ones (no visible key tile), so the barrier phases they
+  // count stay in step across units.
+
   // Registers: the producer / MMA warpgroup gives most of its share to the
-  // two softmax warpgroups (128*80 + 256*208 <= 384*168, the launch total).
+  // two softmax warpgroups (128*104 + 256*184 <= 384*168, the launch total).
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;\n" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
       const uint32_t qfull = bar0 + 8 * kBarQFull;
-      // Packed mode: 3-D box {64 d, Lf rows, pack problems} starting at the
-      // rank's chunk of the unit's first problem.
-      const int32_t pz = static_cast<int32_t>(static_cast<int64_t>(w.bh) * p.pN +
-                                              static_cast<int64_t>(w.g) * p.pack);
       const uint32_t pack_bytes = static_cast<uint32_t>(p.pack * p.Lf) * 128u * C::kChunks;
-      if (p.pack) {
-        mbar_arrive_expect_tx(qfull, pack_bytes);
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sbase + C::kOffQ0 + c * C::kChunkBytes, &tm_q, c * 64, w.rank * p.Lf, pz,
-                      qfull);
-      } else {
-        const int32_t qy = static_cast<int32_t>(w.q_row0 + pair_row0);
-        mbar_arrive_expect_tx(qfull, 2 * C::kQTile);
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_2d(sbase + C::kOffQ0 + c * C::kChunkBytes, &tm_q, c * 64, qy, qfull);
-          tma_load_2d(sbase + C::kOffQ1 + c * C::kChunkBytes, &tm_q, c * 64, qy + kBM, qfull);
-        }
-      }
       const uint64_t keep = l2_policy_evict_last();
-      const int64_t kv_base =
-          static_cast<int64_t>(w.bh) * p.kv_rows_bh + static_cast<int64_t>(w.g) * p.kv_rows_g;
-      int it = 0;
-      TileIter ti;
-      ti.init(p, w);
-      ti.settle(p, w, n_t, gq_max);
+      int it = 0;        // K/V slot sequence over all units
+      int n_loaded = 0;  // Q pairs loaded
       bool ok = true;
-      while (ok && ti.valid(w)) {
-        const int64_t blk = p.kv_own ? static_cast<int64_t>(w.rank) * p.kv_rank_stride +
-                                           static_cast<int64_t>(w.bh) * p.kv_rows_bh
-                                     : kv_base + static_cast<int64_t>(ti.src) * p.L;
-        const int32_t ky = static_cast<int32_t>(blk + static_cast<int64_t>(ti.t) * kBN);
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        const UnitGeo g = unit_geo(p, u);
+        const Unit &w = g.w;
+        TileIter ti;
+        ti.init(p, w);
+        ti.settle(p, w, n_t, g.gq_max);
+        if (!ti.valid(w)) continue;
+        // The previous pair's last QK^T must have read the Q buffers.
+        if (n_loaded > 0 &&
+            !mbar_wait(bar0 + 8 * kBarQEmpty, (n_loaded - 1) & 1, wd, abort_flag))
+          break;
+        // Packed mode: 3-D box {64 d, Lf rows, pack problems} starting at
+        // the rank's chunk of the unit's first problem.
+        const int32_t pz = static_cast<int32_t>(static_cast<int64_t>(w.bh) * p.pN +
+                                                static_cast<int64_t>(w.g) * p.pack);
+        if (p.pack) {
+          mbar_arrive_expect_tx(qfull, g.has_q1 ? 2 * pack_bytes : pack_bytes);
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const int slot = it % C::kSlots;
-          const uint32_t ph = (it / C::kSlots) & 1;
-          if (!mbar_wait(kv_empty0 + 8 * slot, ph ^ 1, wd, abort_flag)) {
-            ok = false;
-            break;
+          for (int c = 0; c < C::kChunks; ++c) {
+            tma_load_3d(sbase + C::kOffQ0 + c * C::kChunkBytes, &tm_q, c * 64, w.rank * p.Lf, pz,
+                        qfull);
+            if (g.has_q1)
+              tma_load_3d(sbase + C::kOffQ1 + c * C::kChunkBytes, &tm_q, c * 64,
+                          (w.rank + 1) * p.Lf, pz, qfull);
           }
-          const CUtensorMap *map = which ? &tm_v : &tm_k;
-          if (p.pack) {
-            mbar_arrive_expect_tx(kv_full0 + 8 * slot, pack_bytes);
+        } else {
+          const int32_t qy = static_cast<int32_t>(w.q_row0 + g.pair_row0);
+          mbar_arrive_expect_tx(qfull, 2 * C::kQTile);
 #pragma unroll
-            for (int c = 0; c < C::kChunks; ++c)
-              tma_load_3d(sbase + C::kOffKV + slot * C::kKVTile + c * C::kChunkBytes, map, c * 64,
-                          ti.src * p.Lf, pz, kv_full0 + 8 * slot);
-          } else {
-            mbar_arrive_expect_tx(kv_full0 + 8 * slot, C::kKVTile);
-#pragma unroll
-            for (int c = 0; c < C::kChunks; ++c)
-              tma_load_2d_hint(sbase + C::kOffKV + slot * C::kKVTile + c * C::kChunkBytes, map,
-                               c * 64, ky, kv_full0 + 8 * slot, keep);
+          for (int c = 0; c < C::kChunks; ++c) {
+            tma_load_2d(sbase + C::kOffQ0 + c * C::kChunkBytes, &tm_q, c * 64, qy, qfull);
+            tma_load_2d(sbase + C::kOffQ1 + c * C::kChunkBytes, &tm_q, c * 64, qy + kBM, qfull);
           }
-          ++it;
         }
-        ++ti.t;
-        ti.settle(p, w, n_t, gq_max);
+        ++n_loaded;
+        const int64_t kv_base =
+            static_cast<int64_t>(w.bh) * p.kv_rows_bh + static_cast<int64_t>(w.g) * p.kv_rows_g;
+        while (ok && ti.valid(w)) {
+          const int64_t blk = p.kv_own ? static_cast<int64_t>(w.rank) * p.kv_rank_stride +
+                                             static_cast<int64_t>(w.bh) * p.kv_rows_bh
+                                       : kv_base + static_cast<int64_t>(ti.src) * p.L;
+          const int32_t ky = static_cast<int32_t>(blk + static_cast<int64_t>(ti.t) * kBN);
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            const int slot = it % C::kSlots;
+            const uint32_t ph = (it / C::kSlots) & 1;
+            if (!mbar_wait(kv_empty0 + 8 * slot, ph ^ 1, wd, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const CUtensorMap *map = which ? &tm_v : &tm_k;
+            if (p.pack) {
+              mbar_arrive_expect_tx(kv_full0 + 8 * slot, pack_bytes);
+#pragma unroll
+              for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(sbase + C::kOffKV + slot * C::kKVTile + c * C::kChunkBytes, map,
+                            c * 64, ti.src * p.Lf, pz, kv_full0 + 8 * slot);
+            } else {
+              mbar_arrive_expect_tx(kv_full0 + 8 * slot, C::kKVTile);
+#pragma unroll
+              for (int c = 0; c < C::kChunks; ++c)
+                tma_load_2d_hint(sbase + C::kOffKV + slot * C::kKVTile + c * C::kChunkBytes, map,
+                                 c * 64, ky, kv_full0 + 8 * slot, keep);
+            }
+            ++it;
+          }
+          ++ti.t;
+          ti.settle(p, w, n_t, g.gq_max);
+        }
       }
       // Drain: every copy issued must land before the CTA may exit.
-      mbar_wait_drain(qfull, 0, p.wd.limit_ns);
+      if (n_loaded > 0) mbar_wait_drain(qfull, (n_loaded - 1) & 1, p.wd.limit_ns);
       for (int i = max(0, it - C::kSlots); i < it; ++i)
         mbar_wait_drain(kv_full0 + 8 * (i % C::kSlots), (i / C::kSlots) & 1, p.wd.limit_ns);
     }
@@ -299,12 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
-      const uint32_t sQ[2] = {sbase + C::kOffQ0, sbase + C::kOffQ1};
-      const int nq = has_q1 ? 2 : 1;
       bool issued = false;
-      TileIter ti;
-      ti.init(p, w);
-      ti.settle(p, w, n_t, gq_max);
       const uint64_t dq[2] = {smem_desc_sw128(sbase + C::kOffQ0, 16, 1024),
                               smem_desc_sw128(sbase + C::kOffQ1, 16, 1024)};
       const uint64_t dk0 = smem_desc_sw128(sbase + C::kOffKV, 16, 1024);
@@ -317,29 +354,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_pv(tmem + col_o(i), tmem + col_s(i),
                  dv0 + static_cast<uint64_t>(slot * (C::kKVTile >> 4)), idesc_o, acc);
       };
-      if (ti.valid(w) && mbar_wait(bar0 + 8 * kBarQFull, 0, wd, abort_flag)) {
+      int it = 0;          // K/V slot sequence: K_j at 2j, V_j at 2j+1 of each unit
+      int n_loaded = 0;    // Q pairs consumed
+      int jt[2] = {0, 0};  // tiles handed to each softmax warpgroup so far
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        const UnitGeo g = unit_geo(p, u);
+        const Unit &w = g.w;
+        const bool has_q1 = g.has_q1;
+        const int nq = has_q1 ? 2 : 1;
+        TileIter ti;
+        ti.init(p, w);
+        ti.settle(p, w, n_t, g.gq_max);
+        if (!ti.valid(w)) continue;
+        if (!(ok = mbar_wait(bar0 + 8 * kBarQFull, n_loaded & 1, wd, abort_flag))) break;
+        ++n_loaded;
         tc_fence_after();
-        int it = 0;  // slot sequence: K_j at 2j, V_j at 2j+1
-        bool ok = mbar_wait(kv_full0 + 8 * (it % C::kSlots), (it / C::kSlots) & 1, wd, abort_flag);
-        if (ok) {
-          tc_fence_after();
-          for (int i = 0; i < nq; ++i) {
-            issue_s(i, it % C::kSlots);
-            mma_commit_e(bar0 + 8 * (kBarSFull + i));
-          }
-          mma_commit_e(kv_empty0 + 8 * (it % C::kSlots));
-          issued = true;
-          ++it;
+        if (!(ok = mbar_wait(kv_full0 + 8 * (it % C::kSlots), (it / C::kSlots) & 1, wd,
+                             abort_flag)))
+          break;
+        tc_fence_after();
+        for (int i = 0; i < nq; ++i) {
+          issue_s(i, it % C::kSlots);
+          mma_commit_e(bar0 + 8 * (kBarSFull + i));
         }
-        for (int j = 0; ok; ++j) {
+        mma_commit_e(kv_empty0 + 8 * (it % C::kSlots));
+        issued = true;
+        ++it;
+        int j = 0;
+        for (;; ++j) {
           const int v_it = it;
           ++ti.t;
-          ti.settle(p, w, n_t, gq_max);
+          ti.settle(p, w, n_t, g.gq_max);
           const bool more = ti.valid(w);
+          // The pair's last QK^T has been issued: the Q buffers are free once
+          // it completes.
+          if (!more) mma_commit_e(bar0 + 8 * kBarQEmpty);
           if (!(ok = mbar_wait(kv_full0 + 8 * (v_it % C::kSlots), (v_it / C::kSlots) & 1, wd,
                                abort_flag)))
             break;
-          if (!(ok = mbar_wait(bar0 + 8 * kBarPFull, j & 1, wd, abort_flag))) break;
+          if (!(ok = mbar_wait(bar0 + 8 * kBarPFull, (jt[0] + j) & 1, wd, abort_flag))) break;
           tc_fence_after();
           issue_o(0, v_it % C::kSlots, j > 0);
           const int k_it = v_it + 1;
@@ -352,7 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit_e(bar0 + 8 * kBarSFull);
           }
           if (has_q1) {
-            if (!(ok = mbar_wait(bar0 + 8 * (kBarPFull + 1), j & 1, wd, abort_flag))) break;
+            if (!(ok = mbar_wait(bar0 + 8 * (kBarPFull + 1), (jt[1] + j) & 1, wd, abort_flag)))
+              break;
             tc_fence_after();
             issue_o(1, v_it % C::kSlots, j > 0);
           }
@@ -365,9 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit_e(kv_empty0 + 8 * (k_it % C::kSlots));
           it = k_it + 1;
         }
-        if (ok) {
-          for (int i = 0; i < nq; ++i) mma_commit_e(bar0 + 8 * (kBarODone + i));
-        }
+        if (!ok) break;
+        it = it + 1;  // the last tile's V slot
+        for (int i = 0; i < nq; ++i) mma_commit_e(bar0 + 8 * (kBarODone + i));
+        jt[0] += j + 1;
+        if (has_q1) jt[1] += j + 1;
       }
       if (issued) {
         // Nothing may still be running on the tensor core when TMEM is freed.
@@ -377,32 +434,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;\n" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory");
     // ------------------------------------------------------------- softmax --
     const int wg = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    if (wg == 0 || has_q1) {
-      const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
-      const uint32_t tS = tmem + lane_bits + col_s(wg);
-      const uint32_t tO = tmem + lane_bits + col_o(wg);
-      const int64_t qi = pair_row0 + wg * kBM + row;  // row within the rank's chunk
+    const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_bits + col_s(wg);
+    const uint32_t tO = tmem + lane_bits + col_o(wg);
+    const float sl2 = p.scale_log2;
+    // Rows start 32-byte aligned when the output and its part stride are
+    // (the entry points only promise 16): then 32-byte stores are used.
+    const bool out_v8 = ((reinterpret_cast<uintptr_t>(p.out) |
+                          static_cast<uintptr_t>(p.out_part_stride * (OUT_F32 ? 4 : 2))) &
+                         31u) == 0;
+    int jt = 0;      // tiles of this warpgroup so far (S_full / P_full phases)
+    int n_done = 0;  // units whose O this warpgroup has read (O_done phases)
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const UnitGeo g = unit_geo(p, u);
+      const Unit &w = g.w;
+      if (!(wg == 0 || g.has_q1)) continue;
+      // Row within the rank's chunk; in packed mode within the tile, whose
+      // rank is w.rank + wg.
+      const int64_t qi = p.pack ? row : g.pair_row0 + wg * kBM + row;
       // Packed mode: row qi is row qi % Lf of problem g * pack + qi / Lf and
       // sees only the keys of that problem (columns [lo, lo + Lf) of a tile).
       const int pr = p.pack ? static_cast<int>(qi / p.Lf) : 0;
       const bool row_valid =
           qi < p.L && (!p.pack || static_cast<int64_t>(w.g) * p.pack + pr < p.pN);
-      const int64_t gq = p.causal ? zz_pos(w.rank, min64(qi, p.L - 1), half, p.P) : 0;
-      const float sl2 = p.scale_log2;
+      const int64_t gq = p.causal ? zz_pos(w.rank, min64(qi, p.L - 1), p.L >> 1, p.P) : 0;
 
       float m_ref = -INFINITY, l = 0.f;
       int j = 0;
       TileIter ti;
       ti.init(p, w);
-      ti.settle(p, w, n_t, gq_max);
+      ti.settle(p, w, n_t, g.gq_max);
       while (ti.valid(w)) {
-        const bool ok =
-            __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarSFull + wg), j & 1, wd, abort_flag));
+        const bool ok = __all_sync(
+            0xffffffffu, mbar_wait(bar0 + 8 * (kBarSFull + wg), (jt + j) & 1, wd, abort_flag));
         if (!ok) break;
         tc_fence_after();
         float s[kBN];
@@ -483,70 +552,95 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar0 + 8 * (kBarPFull + wg));
         ++j;
         ++ti.t;
-        ti.settle(p, w, n_t, gq_max);
+        ti.settle(p, w, n_t, g.gq_max);
       }
       __syncwarp();
       const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
+      if (aborted) break;
       bool have_o = false;
-      if (j > 0 && !aborted) {
-        have_o = __all_sync(0xffffffffu,
-                            mbar_wait(bar0 + 8 * (kBarODone + wg), 0, wd, abort_flag));
+      if (j > 0) {
+        have_o = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarODone + wg), n_done & 1, wd,
+                                                   abort_flag));
+        ++n_done;
+        if (!have_o) break;
         tc_fence_after();
       }
-      if (!aborted) {
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-        const float lse_val = (l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
-        const int part = p.part_by_block ? ((w.rank - w.s_lo) % p.P + p.P) % p.P : w.part;
-        const int64_t orow =
-            p.pack ? (static_cast<int64_t>(w.bh) * p.pN + static_cast<int64_t>(w.g) * p.pack + pr) *
-                             p.pT + static_cast<int64_t>(w.rank) * p.Lf + (qi - static_cast<int64_t>(pr) * p.Lf)
-                   : w.q_row0 + qi;
-        if (OUT_F32) {
-          float *out = reinterpret_cast<float *>(p.out) + part * p.out_part_stride + orow * D;
+      jt += j;
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const float lse_val = (l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+      const int part = p.part_by_block ? ((w.rank - w.s_lo) % p.P + p.P) % p.P : w.part;
+      const int64_t orow =
+          p.pack ? (static_cast<int64_t>(w.bh) * p.pN + static_cast<int64_t>(w.g) * p.pack + pr) *
+                           p.pT +
+                       static_cast<int64_t>(w.rank + wg) * p.Lf + (qi - static_cast<int64_t>(pr) * p.Lf)
+                 : w.q_row0 + qi;
+      if (OUT_F32) {
+        float *out = reinterpret_cast<float *>(p.out) + part * p.out_part_stride + orow * D;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            if (have_o) {
-              tmem_ld32(tO + c * 32, o);
-              tmem_wait_ld();
-            } else {
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          if (have_o) {
+            tmem_ld32(tO + c * 32, o);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-              for (int x = 0; x < 32; ++x) o[x] = 0.f;
-            }
-            if (row_valid) {
-              float4 *dst = reinterpret_cast<float4 *>(out + c * 32);
-#pragma unroll
-              for (int x = 0; x < 8; ++x)
-                dst[x] = make_float4(o[4 * x] * inv_l, o[4 * x + 1] * inv_l, o[4 * x + 2] * inv_l,
-                                     o[4 * x + 3] * inv_l);
-            }
+            for (int x = 0; x < 32; ++x) o[x] = 0.f;
           }
-        } else {
-          __nv_bfloat16 *out =
-              reinterpret_cast<__nv_bfloat16 *>(p.out) + part * p.out_part_stride + orow * D;
+          if (row_valid && out_v8) {
+            // 32-byte stores: every lane writes whole L2 sectors of its row.
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            if (have_o) {
-              tmem_ld32(tO + c * 32, o);
-              tmem_wait_ld();
-            } else {
+            for (int x = 0; x < 4; ++x) {
+              uint32_t v8[8];
 #pragma unroll
-              for (int x = 0; x < 32; ++x) o[x] = 0.f;
+              for (int y = 0; y < 8; ++y) v8[y] = __float_as_uint(o[8 * x + y] * inv_l);
+              st_global_v8(out + c * 32 + 8 * x, v8);
             }
-            if (row_valid) {
-              uint4 *dst = reinterpret_cast<uint4 *>(out + c * 32);
+          } else if (row_valid) {
+            float4 *dst = reinterpret_cast<float4 *>(out + c * 32);
 #pragma unroll
-              for (int x = 0; x < 4; ++x)
-                dst[x] = make_uint4(pack_bf16x2(o[8 * x] * inv_l, o[8 * x + 1] * inv_l),
-                                    pack_bf16x2(o[8 * x + 2] * inv_l, o[8 * x + 3] * inv_l),
-                                    pack_bf16x2(o[8 * x + 4] * inv_l, o[8 * x + 5] * inv_l),
-                                    pack_bf16x2(o[8 * x + 6] * inv_l, o[8 * x + 7] * inv_l));
-            }
+            for (int x = 0; x < 8; ++x)
+              dst[x] = make_float4(o[4 * x] * inv_l, o[4 * x + 1] * inv_l, o[4 * x + 2] * inv_l,
+                                   o[4 * x + 3] * inv_l);
           }
         }
-        if (row_valid) p.lse[part * p.lse_part_stride + orow] = lse_val;
+      } else {
+        __nv_bfloat16 *out =
+            reinterpret_cast<__nv_bfloat16 *>(p.out) + part * p.out_part_stride + orow * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          if (have_o) {
+            tmem_ld32(tO + c * 32, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = 0.f;
+          }
+          if (row_valid && out_v8) {
+            // 32-byte stores: every lane writes whole L2 sectors of its row.
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              uint32_t v8[8];
+#pragma unroll
+              for (int y = 0; y < 8; ++y)
+                v8[y] = pack_bf16x2(o[16 * x + 2 * y] * inv_l, o[16 * x + 2 * y + 1] * inv_l);
+              st_global_v8(out + c * 32 + 16 * x, v8);
+            }
+          } else if (row_valid) {
+            uint4 *dst = reinterpret_cast<uint4 *>(out + c * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              dst[x] = make_uint4(pack_bf16x2(o[8 * x] * inv_l, o[8 * x + 1] * inv_l),
+                                  pack_bf16x2(o[8 * x + 2] * inv_l, o[8 * x + 3] * inv_l),
+                                  pack_bf16x2(o[8 * x + 4] * inv_l, o[8 * x + 5] * inv_l),
+                                  pack_bf16x2(o[8 * x + 6] * inv_l, o[8 * x + 7] * inv_l));
+          }
+        }
       }
+      if (row_valid) p.lse[part * p.lse_part_stride + orow] = lse_val;
+      // O of this unit has been read into registers: the next unit's first
+      // PV (accumulate off) may overwrite it once this warpgroup's next
+      // P_full arrival, which follows these loads, has been seen.
     }
   }
 
@@ -558,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
 }
+
 
 // A kernel whose only wait can never complete (nothing arrives on the
 // barrier): exercises the bounded-wait path.
@@ -642,8 +737,21 @@ cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const C
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  ring_attn_kernel<D, OUT_F32><<<static_cast<unsigned>(n_units), kThreads, C::kSmemBytes, stream>>>(
-      mq, mk, mv, p);
+  // Short units (a few key tiles each: 900-token frames, packed temporal
+  // problems) run persistently, one CTA per SM walking units blockIdx.x,
+  // + gridDim.x, ..., so that a CTA's next query pair and key tiles load
+  // while its current pair finishes.  Long units get one CTA each and the
+  // block scheduler balances them (static striding costs ~1% there).
+  static int sms[64] = {};
+  if (sms[dev] == 0) {
+    e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t tiles_per_unit = ((p.L + kBN - 1) / kBN) * p.steps_per_group;
+  const int64_t grid =
+      (tiles_per_unit <= kPersistMaxTiles && n_units > sms[dev]) ? sms[dev] : n_units;
+  ring_attn_kernel<D, OUT_F32><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
+      mq, mk, mv, p, static_cast<int>(n_units));
   return cudaGetLastError();
 }
 

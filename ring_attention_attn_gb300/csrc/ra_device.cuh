@@ -257,6 +257,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// One 32-byte global store (a full L2 sector per lane); addr 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *addr, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(addr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // ------------------------------------------------- TMEM-operand MMA, math --
 // Packed fp32x2 arithmetic (two values per instruction) and 3-input max
 // (sm_100 family).

@@ -38,6 +38,11 @@ struct AttnParams {
   // G = ceil(pN / pack), and a query only sees keys of its own problem.
   int pack, Lf, pT;
   int64_t pN;
+  // Packed mode only: when pack_ranks > 0 a unit holds the chunks of two
+  // consecutive ranks (2 * unit index and the next, below pack_ranks) as its
+  // two query tiles; n_ranks then counts rank pairs.  Both tiles meet the
+  // same key/value tiles, in the first rank's ring order.
+  int pack_ranks;
   // Per-rank K/V buffers (overlapped ring): when kv_own != 0, rank r's
   // current block for head bh is rows [r * kv_rank_stride + bh * kv_rows_bh,
   // + L) of the K/V tensors, whatever block of the ring it holds.

@@ -184,6 +184,67 @@ def test_rank_partials_and_merge(causal):
     assert (merged.float() - fused.float()).abs().max().item() <= 4e-3
 
 
+def test_persistent_units_with_empty_steps():
+    """Short units (4 key tiles) and more units than SMs: CTAs walk several
+    units each.  Causal zigzag per-step partials of rank 0 make the pairs of
+    its first chunk empty for every block but its own (they see no key), so
+    the walk mixes empty and full units; every partial, merged, must match
+    the oracle."""
+    B, H, S, d, P, rank = 1, 40, 4096, 128, 8, 0
+    q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=91)
+    qs, ks, vs = (_shard_host(x, P, 1) for x in (q, k, v))
+    L = S // P
+    q_local = qs[:, :, rank * L:(rank + 1) * L].contiguous().cuda()
+    parts, lparts = ra.ring_attn_fwd_rank(q_local, ks.cuda(), vs.cuda(), P, rank, causal=True,
+                                          out_fp32=True)
+    merged, lmerged = ra.lse_merge(parts, lparts)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+    # first chunk of rank 0 (global tokens 0..255) sees only its own block
+    C = S // (2 * P)
+    lp = lparts.cpu()
+    assert torch.isinf(lp[1:, :, :, :C]).all() and (lp[1:, :, :, :C] < 0).all()
+    assert (parts.cpu()[1:, :, :, :C] == 0).all()
+    s2g, _ = oracle.shard_index(S, P, 1)
+    gq = s2g[rank * L:(rank + 1) * L]
+    pick = np.array([0, 1, C - 1, C, C + 1, L - 1, 77, 300])
+    rows = oracle.flat_rows(B, H, S, gq[pick])
+    ro, rl = oracle.attention(q, k, v, causal=True, rows=rows)
+    mo = merged.reshape(B, H, L, d)[:, :, torch.from_numpy(pick)].reshape(-1, d)
+    ml = lmerged.reshape(B, H, L)[:, :, torch.from_numpy(pick)].reshape(-1)
+    _cmp(mo, ml, ro, rl)
+
+
+@pytest.mark.parametrize("out_fp32", [False, True])
+def test_outputs_at_16_byte_offsets(out_fp32):
+    """Outputs that are only 16-byte aligned take the 16-byte store path;
+    the values must equal those written to aligned buffers bit for bit."""
+    B, H, S, d, P = 1, 2, 1000, 128, 4
+    q, k, v = (x.cuda() for x in synth.make_custom((B, H, S, d), (B, H, S, d), seed=123))
+    if out_fp32:
+        L = S // P
+        ql = q[:, :, :L].contiguous()
+        want, lwant = ra.ring_attn_fwd_rank(ql, k, v, P, 0, out_fp32=True)
+        buf = torch.empty(want.numel() + 4, dtype=torch.float32, device="cuda")
+        lbuf = torch.empty(lwant.numel() + 4, dtype=torch.float32, device="cuda")
+        got = buf[4:].view(want.shape)
+        lgot = lbuf[4:].view(lwant.shape)
+        assert got.data_ptr() % 32 == 16
+        ra.ring_attn_fwd_rank(ql, k, v, P, 0, out_fp32=True, out=got, lse=lgot)
+    else:
+        want, lwant = ra.ring_attn_fwd(q, k, v, P)
+        buf = torch.empty(want.numel() + 8, dtype=torch.bfloat16, device="cuda")
+        lbuf = torch.empty(lwant.numel() + 4, dtype=torch.float32, device="cuda")
+        got = buf[8:].view(want.shape)
+        lgot = lbuf[4:].view(lwant.shape)
+        assert got.data_ptr() % 32 == 16
+        ra.ring_attn_fwd(q, k, v, P, out=got, lse=lgot)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+    assert torch.equal(got, want)
+    assert torch.equal(lgot, lwant)
+
+
 def test_rank_step_subrange():
     B, H, S, d, P, rank = 1, 1, 2048, 64, 4, 2
     q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=77)
@@ -290,9 +351,12 @@ def test_allgather_reducescatter_forms_match_oracle(form, B, H, S, d, P, causal)
 
 
 # ---------------------------------------------------------------- factored --
-def test_factored_small_full():
-    B, H, T, N, d, P = 1, 2, 8, 50, 64, 4
-    q, k, v = synth.make_custom((B, H, T * N, d), (B, H, T * N, d), seed=99)
+@pytest.mark.parametrize("B,H,T,N,d,P", [(1, 2, 8, 50, 64, 4),    # 2 rank pairs
+                                          (1, 2, 12, 50, 64, 3),   # odd P: last rank unpaired
+                                          (2, 1, 6, 70, 128, 1),   # one rank
+                                          (1, 3, 24, 40, 128, 2)])
+def test_factored_small_full(B, H, T, N, d, P):
+    q, k, v = synth.make_custom((B, H, T * N, d), (B, H, T * N, d), seed=99 + T + P)
     os_, ls, ot, lt = ra.factored_attn(q.cuda(), k.cuda(), v.cuda(), T, N, P)
     torch.cuda.synchronize()
     assert ra.ra_get_status() == 0
