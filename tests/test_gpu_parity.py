@@ -184,14 +184,15 @@ def test_rank_partials_and_merge(causal):
     assert (merged.float() - fused.float()).abs().max().item() <= 4e-3
 
 
-def test_persistent_units_with_empty_steps():
+@pytest.mark.parametrize("d", [64, 128])
+def test_persistent_units_with_empty_steps(d):
     """Short units (4 key tiles) and more units than SMs: CTAs walk several
     units each.  Causal zigzag per-step partials of rank 0 make the pairs of
     its first chunk empty for every block but its own (they see no key), so
     the walk mixes empty and full units; every partial, merged, must match
     the oracle."""
-    B, H, S, d, P, rank = 1, 40, 4096, 128, 8, 0
-    q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=91)
+    B, H, S, P, rank = 1, 40, 4096, 8, 0
+    q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=91 + d)
     qs, ks, vs = (_shard_host(x, P, 1) for x in (q, k, v))
     L = S // P
     q_local = qs[:, :, rank * L:(rank + 1) * L].contiguous().cuda()
