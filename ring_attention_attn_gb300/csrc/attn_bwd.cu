@@ -12,16 +12,20 @@
 //
 // Three kernels:
 //   bwd_prep_kernel   D_i = dO_i . O_i (fp32), one warp per row.
-//   bwd_dq_kernel     one 128-row query tile per CTA.  Per K/V tile:
-//                     S = Q K^T and dP = dO V^T (SMEM operands) into TMEM;
-//                     the compute warpgroup writes dS (bf16) over S's first 64
-//                     columns; dQ += dS K takes dS from TMEM.
-//   bwd_dkv_kernel    one 128-key tile per CTA.  Per query tile:
-//                     S^T = K Q^T and dP^T = V dO^T; the compute warpgroup
-//                     writes P^T over S^T and dS^T over dP^T (bf16);
-//                     dV += P^T dO and dK += dS^T Q take them from TMEM.
-// Roles (256 threads): warp 0 TMA producer, warp 1 TMEM allocation and
-// elected MMA issue, warps 4..7 one thread per row of the tile.
+//   bwd_dq_kernel     one 128-row query tile per CTA.  Per K/V tile, in two
+//                     halves of 64 keys: S_h = Q K_h^T and dP_h = dO V_h^T
+//                     (SMEM operands) into TMEM; compute warpgroup h writes
+//                     dS_h (bf16) over S_h; dQ += dS_h K_h takes it from TMEM.
+//   bwd_dkv_kernel    one 128-key tile per CTA.  Per query tile, in two
+//                     halves of 64 queries: S^T_h = K Q_h^T and
+//                     dP^T_h = V dO_h^T; compute warpgroup h writes P^T_h
+//                     over S^T_h and dS^T_h over dP^T_h (bf16);
+//                     dV += P^T_h dO_h and dK += dS^T_h Q_h take them from TMEM.
+// Roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocation and
+// elected MMA issue, warps 4..7 / 8..11 compute warpgroups 0 / 1, one thread
+// per row of the tile and half h of its columns.  The halves pipeline: while
+// warpgroup h works on half h of tile j, the tensor core runs the other
+// half's products and half h's MMAs of tile j+1 wait only for it.
 #include <math.h>
 
 #include "attn_common.cuh"
@@ -31,10 +35,10 @@
 namespace ra {
 namespace {
 
-constexpr int kThreadsB = 256;
+constexpr int kThreadsB = 384;
 constexpr float kLog2eB = 1.44269504088896340736f;
 
-constexpr int kBKVFirst = 8;
+constexpr int kBKVFirst = 11;
 
 template <int D>
 struct BCfg {
@@ -48,14 +52,17 @@ struct BCfg {
   static constexpr int kOffKV = 2 * kTile;  // ring of streamed tiles
   static constexpr int kOffBar = kOffKV + kSlots * kTile;
   static constexpr int kBarBytes = 512;
-  static constexpr int kOffLD = kOffBar + kBarBytes;  // 2 x (LSE[128], D[128]) fp32
+  static constexpr int kOffLD = kOffBar + kBarBytes;  // [half][buffer](LSE[64], D[64]) fp32
   static constexpr int kLDBytes = 2048;
   static constexpr int kSmemBytes = kOffLD + kLDBytes + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(8 * (kBKVFirst + 2 * kSlots) <= 496, "barriers overlap the TMEM slot");
 };
 
-enum : int { kBA = 0, kBS = 1, kBP = 2, kBO = 3, kBDrain = 4, kBLd = 5, kBKV = 8 };  // kBLd: +0/+1
+// Barriers: fixed tiles loaded, half h of S/dP ready (+h), half h computed
+// (+h, 128 arrivals), accumulators done, drain, the dK/dV kernel's LSE/D
+// staging (+2h + buffer, 128 arrivals), then full/empty per ring slot.
+enum : int { kBA = 0, kBH = 1, kBC = 3, kBO = 5, kBDrain = 6, kBLd = 7, kBKV = kBKVFirst };
 constexpr int kBTmemSlot = 496;
 constexpr int kBAbort = 500;
 constexpr uint32_t kColS = 0, kColP = 128, kColAcc0 = 256, kColAcc1 = 384;
@@ -135,6 +142,19 @@ __device__ __forceinline__ BBars init_bars(uint32_t sbase) {
   return r;
 }
 
+// Half-tile MMA issue: an accumulation over 64 rows of the streamed tile
+// (K = 64: four MMAs of 16) with A (bf16 pairs) from TMEM and B MN-major.
+__device__ __forceinline__ void issue_acc_k64(uint32_t d_tmem, uint32_t a_tmem, uint64_t db,
+                                              uint32_t idesc, bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    mma_ts_e(d_tmem, a_tmem + kk * 8, db + static_cast<uint64_t>(kk * (2048 >> 4)), idesc,
+             (acc || kk > 0) ? 1u : 0u);
+}
+
+// Descriptor offset of row 64 of a 128-row, 128-byte-swizzled tile.
+constexpr uint64_t kHalfRows = (64 * 128) >> 4;
+
 // ------------------------------------------------------------------ dQ ----
 template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1)
@@ -170,8 +190,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bb.b(kBA), 1);
-    mbar_init(bb.b(kBS), 1);
-    mbar_init(bb.b(kBP), 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bb.b(kBH + h), 1);
+      mbar_init(bb.b(kBC + h), 128);
+    }
     mbar_init(bb.b(kBO), 1);
     mbar_init(bb.b(kBDrain), 1);
     for (int s = 0; s < C::kSlots; ++s) {
@@ -219,47 +241,79 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         mbar_wait_drain(bb.kv_full0 + 8 * (i % C::kSlots), (i / C::kSlots) & 1, p.wd.limit_ns);
     }
   } else if (warp == 1) {
-    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t idesc_h = idesc_bf16_f32(128, 64, 0, 0);
     constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
     constexpr uint32_t kSlotDesc = C::kTile >> 4;
     const uint64_t dQd = smem_desc_sw128(sbase + C::kOffA, 16, 1024);
     const uint64_t dOd = smem_desc_sw128(sbase + C::kOffB, 16, 1024);
     const uint64_t dKV = smem_desc_sw128(sbase + C::kOffKV, 16, 1024);
     const uint64_t dKVmn = smem_desc_sw128(sbase + C::kOffKV, C::kChunkBytes, 1024);
-    bool issued = false;
+    // S_h = Q K_h^T and dP_h = dO V_h^T for the 64 keys of half h of the
+    // K/V tiles in slots ks, vs.
+    auto issue_s = [&](int h, int ks, int vs) {
+      issue_qk<D>(tmem + kColS + 64 * h, dQd,
+                  dKV + static_cast<uint64_t>(ks * kSlotDesc) + h * kHalfRows, idesc_h);
+      issue_qk<D>(tmem + kColP + 64 * h, dOd,
+                  dKV + static_cast<uint64_t>(vs * kSlotDesc) + h * kHalfRows, idesc_h);
+      mma_commit_e(bb.b(kBH + h));
+    };
+    bool issued = false, ok = true;
     BIter ti = make_iter();
     if (ti.valid() && mbar_wait(bb.b(kBA), 0, wd, abort_flag)) {
       tc_fence_after();
-      int it = 0;
-      for (int j = 0; ti.valid(); ++j, it += 2, ++ti.t, ti.settle()) {
-        const int ks = it % C::kSlots, vs = (it + 1) % C::kSlots;
-        if (!mbar_wait(bb.kv_full0 + 8 * ks, (it / C::kSlots) & 1, wd, abort_flag)) break;
-        if (!mbar_wait(bb.kv_full0 + 8 * vs, ((it + 1) / C::kSlots) & 1, wd, abort_flag)) break;
+      int it = 0;  // K_j in slot it, V_j in it + 1
+      ok = mbar_wait(bb.kv_full0 + 8 * (it % C::kSlots), (it / C::kSlots) & 1, wd, abort_flag) &&
+           mbar_wait(bb.kv_full0 + 8 * ((it + 1) % C::kSlots), ((it + 1) / C::kSlots) & 1, wd,
+                     abort_flag);
+      if (ok) {
         tc_fence_after();
-        issue_qk<D>(tmem + kColS, dQd, dKV + static_cast<uint64_t>(ks * kSlotDesc), idesc_s);
-        issue_qk<D>(tmem + kColP, dOd, dKV + static_cast<uint64_t>(vs * kSlotDesc), idesc_s);
-        mma_commit_e(bb.b(kBS));
-        mma_commit_e(bb.kv_empty0 + 8 * vs);
+        issue_s(0, it % C::kSlots, (it + 1) % C::kSlots);
+        issue_s(1, it % C::kSlots, (it + 1) % C::kSlots);
+        mma_commit_e(bb.kv_empty0 + 8 * ((it + 1) % C::kSlots));  // V_0: last use issued
         issued = true;
-        if (!mbar_wait(bb.b(kBP), j & 1, wd, abort_flag)) break;
-        tc_fence_after();
-        // dQ += dS K: dS over S's columns, K MN-major (d contiguous).
-        issue_pv(tmem + kColAcc0, tmem + kColS, dKVmn + static_cast<uint64_t>(ks * kSlotDesc),
-                 idesc_o, j > 0);
-        mma_commit_e(bb.kv_empty0 + 8 * ks);
       }
-      if (!*abort_flag) mma_commit_e(bb.b(kBO));
+      for (int j = 0; ok; ++j) {
+        const int ks = it % C::kSlots;
+        const int nk = it + 2;
+        ++ti.t;
+        ti.settle();
+        const bool more = ti.valid();
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!(ok = mbar_wait(bb.b(kBC + h), j & 1, wd, abort_flag))) break;
+          tc_fence_after();
+          // dQ += dS_h K_h: dS_h over S_h's columns, K MN-major (d contiguous).
+          issue_acc_k64(tmem + kColAcc0, tmem + kColS + 64 * h,
+                        dKVmn + static_cast<uint64_t>(ks * kSlotDesc) + h * kHalfRows, idesc_o,
+                        j > 0 || h > 0);
+          if (h == 1) mma_commit_e(bb.kv_empty0 + 8 * ks);  // K_j: last use issued
+          if (more) {
+            if (h == 0) {
+              ok = mbar_wait(bb.kv_full0 + 8 * (nk % C::kSlots), (nk / C::kSlots) & 1, wd,
+                             abort_flag) &&
+                   mbar_wait(bb.kv_full0 + 8 * ((nk + 1) % C::kSlots), ((nk + 1) / C::kSlots) & 1,
+                             wd, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_s(h, nk % C::kSlots, (nk + 1) % C::kSlots);
+            if (h == 1) mma_commit_e(bb.kv_empty0 + 8 * ((nk + 1) % C::kSlots));  // V_{j+1}
+          }
+        }
+        if (!ok || !more) break;
+        it = nk;
+      }
+      if (ok) mma_commit_e(bb.b(kBO));
     }
     if (issued) {
       mma_commit_e(bb.b(kBDrain));
       mbar_wait_drain(bb.b(kBDrain), 0, p.wd.limit_ns);
     }
   } else if (warp >= 4) {
+    const int h = (warp - 4) >> 2;  // half of the key tile this warpgroup handles
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_bits + kColS, tP = tmem + lane_bits + kColP;
-    const uint32_t tQ = tmem + lane_bits + kColAcc0;
+    const uint32_t tS = tmem + lane_bits + kColS + 64 * h, tP = tmem + lane_bits + kColP + 64 * h;
     const bool valid = row < nq;
     const int64_t grow = q_row0 + row;
     const float lse2 = valid ? p.lse[grow] * kLog2eB : 0.f;
@@ -268,13 +322,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const float sl2 = p.scale_log2;
     int j = 0;
     for (BIter ti = make_iter(); ti.valid(); ++j, ++ti.t, ti.settle()) {
-      if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBS), j & 1, wd, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBH + h), j & 1, wd, abort_flag))) break;
       tc_fence_after();
       const int64_t k0 = static_cast<int64_t>(ti.t) * 128;
       int nvis = static_cast<int>(min64(128, p.L - k0));
       if (p.causal) nvis = causal_visible(ti.blk, k0, gq, p.L, p.P);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float sv[32], pv[32];
         tmem_ld32(tS + c * 32, sv);
         tmem_ld32(tP + c * 32, pv);
@@ -282,7 +336,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
-          const int cc = c * 32 + 2 * x;
+          const int cc = 64 * h + c * 32 + 2 * x;
           const float p0 = cc < nvis ? ex2(fmaf(sv[2 * x], sl2, -lse2)) : 0.f;
           const float p1 = cc + 1 < nvis ? ex2(fmaf(sv[2 * x + 1], sl2, -lse2)) : 0.f;
           pk[x] = pack_bf16x2(p0 * (pv[2 * x] - Drow), p1 * (pv[2 * x + 1] - Drow));
@@ -291,15 +345,17 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bb.b(kBP));
+      mbar_arrive(bb.b(kBC + h));
     }
     __syncwarp();
     const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
     if (!aborted) {
       const bool have = j > 0 && __all_sync(0xffffffffu, mbar_wait(bb.b(kBO), 0, wd, abort_flag));
       tc_fence_after();
+      // Warpgroup h writes columns [h D/2, (h+1) D/2) of its dQ rows.
+      const uint32_t tQ = tmem + lane_bits + kColAcc0 + (D / 2) * h;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         float o[32];
         if (have) {
           tmem_ld32(tQ + c * 32, o);
@@ -308,7 +364,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] = 0.f;
         }
-        if (valid) store_row_bf16(p.dq + grow * D + c * 32, o, p.scale);
+        if (valid) store_row_bf16(p.dq + grow * D + (D / 2) * h + c * 32, o, p.scale);
       }
     }
   }
@@ -335,7 +391,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const BBars bb = init_bars<D>(sbase);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffBar + kBAbort);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + kBTmemSlot);
-  float *sm_ld = reinterpret_cast<float *>(smem + C::kOffLD);  // [2][LSE 128 | D 128]
+  float *sm_ld = reinterpret_cast<float *>(smem + C::kOffLD);  // [half][buffer](LSE 64 | D 64)
   const Watchdog wd{p.wd.status, p.wd.limit_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -357,12 +413,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bb.b(kBA), 1);
-    mbar_init(bb.b(kBS), 1);
-    mbar_init(bb.b(kBP), 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bb.b(kBH + h), 1);
+      mbar_init(bb.b(kBC + h), 128);
+      mbar_init(bb.b(kBLd + 2 * h), 128);
+      mbar_init(bb.b(kBLd + 2 * h + 1), 128);
+    }
     mbar_init(bb.b(kBO), 1);
     mbar_init(bb.b(kBDrain), 1);
-    mbar_init(bb.b(kBLd), 128);
-    mbar_init(bb.b(kBLd + 1), 128);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(bb.kv_full0 + 8 * s, 1);
       mbar_init(bb.kv_empty0 + 8 * s, 1);
@@ -408,75 +466,114 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         mbar_wait_drain(bb.kv_full0 + 8 * (i % C::kSlots), (i / C::kSlots) & 1, p.wd.limit_ns);
     }
   } else if (warp == 1) {
-    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t idesc_h = idesc_bf16_f32(128, 64, 0, 0);
     constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
     constexpr uint32_t kSlotDesc = C::kTile >> 4;
     const uint64_t dKd = smem_desc_sw128(sbase + C::kOffA, 16, 1024);
     const uint64_t dVd = smem_desc_sw128(sbase + C::kOffB, 16, 1024);
     const uint64_t dRing = smem_desc_sw128(sbase + C::kOffKV, 16, 1024);
     const uint64_t dRingMn = smem_desc_sw128(sbase + C::kOffKV, C::kChunkBytes, 1024);
-    bool issued = false;
+    // S^T_h = K Q_h^T and dP^T_h = V dO_h^T (rows = keys, 64 query columns)
+    // for half h of the Q / dO tiles in slots qs, gs.
+    auto issue_s = [&](int h, int qs, int gs) {
+      issue_qk<D>(tmem + kColS + 64 * h, dKd,
+                  dRing + static_cast<uint64_t>(qs * kSlotDesc) + h * kHalfRows, idesc_h);
+      issue_qk<D>(tmem + kColP + 64 * h, dVd,
+                  dRing + static_cast<uint64_t>(gs * kSlotDesc) + h * kHalfRows, idesc_h);
+      mma_commit_e(bb.b(kBH + h));
+    };
+    bool issued = false, ok = true;
     BIter ti = make_iter();
     if (ti.valid() && mbar_wait(bb.b(kBA), 0, wd, abort_flag)) {
       tc_fence_after();
-      int it = 0;
-      for (int j = 0; ti.valid(); ++j, it += 2, ++ti.t, ti.settle()) {
-        const int qs = it % C::kSlots, gs = (it + 1) % C::kSlots;
-        if (!mbar_wait(bb.kv_full0 + 8 * qs, (it / C::kSlots) & 1, wd, abort_flag)) break;
-        if (!mbar_wait(bb.kv_full0 + 8 * gs, ((it + 1) / C::kSlots) & 1, wd, abort_flag)) break;
+      int it = 0;  // Q_j in slot it, dO_j in it + 1
+      ok = mbar_wait(bb.kv_full0 + 8 * (it % C::kSlots), (it / C::kSlots) & 1, wd, abort_flag) &&
+           mbar_wait(bb.kv_full0 + 8 * ((it + 1) % C::kSlots), ((it + 1) / C::kSlots) & 1, wd,
+                     abort_flag);
+      if (ok) {
         tc_fence_after();
-        // S^T = K Q^T and dP^T = V dO^T (rows = keys, columns = queries).
-        issue_qk<D>(tmem + kColS, dKd, dRing + static_cast<uint64_t>(qs * kSlotDesc), idesc_s);
-        issue_qk<D>(tmem + kColP, dVd, dRing + static_cast<uint64_t>(gs * kSlotDesc), idesc_s);
-        mma_commit_e(bb.b(kBS));
+        issue_s(0, it % C::kSlots, (it + 1) % C::kSlots);
+        issue_s(1, it % C::kSlots, (it + 1) % C::kSlots);
         issued = true;
-        if (!mbar_wait(bb.b(kBP), j & 1, wd, abort_flag)) break;
-        tc_fence_after();
-        // dV += P^T dO and dK += dS^T Q (dO, Q MN-major).
-        issue_pv(tmem + kColAcc0, tmem + kColS, dRingMn + static_cast<uint64_t>(gs * kSlotDesc),
-                 idesc_o, j > 0);
-        issue_pv(tmem + kColAcc1, tmem + kColP, dRingMn + static_cast<uint64_t>(qs * kSlotDesc),
-                 idesc_o, j > 0);
-        mma_commit_e(bb.kv_empty0 + 8 * qs);
-        mma_commit_e(bb.kv_empty0 + 8 * gs);
       }
-      if (!*abort_flag) mma_commit_e(bb.b(kBO));
+      for (int j = 0; ok; ++j) {
+        const int qs = it % C::kSlots, gs = (it + 1) % C::kSlots;
+        const int nx = it + 2;
+        ++ti.t;
+        ti.settle();
+        const bool more = ti.valid();
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!(ok = mbar_wait(bb.b(kBC + h), j & 1, wd, abort_flag))) break;
+          tc_fence_after();
+          // dV += P^T_h dO_h and dK += dS^T_h Q_h (dO, Q MN-major).
+          issue_acc_k64(tmem + kColAcc0, tmem + kColS + 64 * h,
+                        dRingMn + static_cast<uint64_t>(gs * kSlotDesc) + h * kHalfRows, idesc_o,
+                        j > 0 || h > 0);
+          issue_acc_k64(tmem + kColAcc1, tmem + kColP + 64 * h,
+                        dRingMn + static_cast<uint64_t>(qs * kSlotDesc) + h * kHalfRows, idesc_o,
+                        j > 0 || h > 0);
+          if (h == 1) {
+            mma_commit_e(bb.kv_empty0 + 8 * qs);  // Q_j and dO_j: last uses issued
+            mma_commit_e(bb.kv_empty0 + 8 * gs);
+          }
+          if (more) {
+            if (h == 0) {
+              ok = mbar_wait(bb.kv_full0 + 8 * (nx % C::kSlots), (nx / C::kSlots) & 1, wd,
+                             abort_flag) &&
+                   mbar_wait(bb.kv_full0 + 8 * ((nx + 1) % C::kSlots), ((nx + 1) / C::kSlots) & 1,
+                             wd, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_s(h, nx % C::kSlots, (nx + 1) % C::kSlots);
+          }
+        }
+        if (!ok || !more) break;
+        it = nx;
+      }
+      if (ok) mma_commit_e(bb.b(kBO));
     }
     if (issued) {
       mma_commit_e(bb.b(kBDrain));
       mbar_wait_drain(bb.b(kBDrain), 0, p.wd.limit_ns);
     }
   } else if (warp >= 4) {
+    const int h = (warp - 4) >> 2;  // half of the query tile this warpgroup handles
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // key row of the tile
+    const int row = quarter * 32 + lane;  // key row of the tile; thread index in the warpgroup
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_bits + kColS, tP = tmem + lane_bits + kColP;
-    const uint32_t tV = tmem + lane_bits + kColAcc0, tK = tmem + lane_bits + kColAcc1;
+    const uint32_t tS = tmem + lane_bits + kColS + 64 * h, tP = tmem + lane_bits + kColP + 64 * h;
     const bool kvalid = row < nk;
     const int64_t gk = p.causal ? zz_pos(b, min64(k0 + row, p.L - 1), C2, p.P) : 0;
     const float sl2 = p.scale_log2;
     int j = 0;
     for (BIter ti = make_iter(); ti.valid(); ++j, ++ti.t, ti.settle()) {
-      // This query tile's LSE (log2 units) and D, double-buffered in SMEM.
-      float *ld = sm_ld + (j & 1) * 256;
+      // LSE (log2 units) and D of this half's 64 queries, double-buffered.
+      float *ld = sm_ld + (2 * h + (j & 1)) * 128;
       const int64_t q0 = static_cast<int64_t>(ti.t) * 128;
       const int64_t nq = min64(128, p.L - q0);
-      const int64_t qrow = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(ti.blk) * p.L + q0 + row;
-      // Buffer j&1 was last read two tiles ago; no thread can still be there,
-      // since this tile's S needs every thread's arrival for the previous one.
-      ld[row] = row < nq ? p.lse[qrow] * kLog2eB : 0.f;
-      ld[128 + row] = row < nq ? p.Dv[qrow] : 0.f;
-      mbar_arrive(bb.b(kBLd + (j & 1)));  // release: the values above
-      if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBLd + (j & 1)), (j >> 1) & 1, wd, abort_flag)))
+      const int64_t qrow0 =
+          static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(ti.blk) * p.L + q0 + 64 * h;
+      // Buffer (h, j&1) was last read two tiles ago; no thread of this
+      // warpgroup can still be there, since half h of this tile's S^T needs
+      // every one of its arrivals for the previous tile.
+      const int qi = row & 63;
+      if (row < 64)
+        ld[qi] = 64 * h + qi < nq ? p.lse[qrow0 + qi] * kLog2eB : 0.f;
+      else
+        ld[64 + qi] = 64 * h + qi < nq ? p.Dv[qrow0 + qi] : 0.f;
+      mbar_arrive(bb.b(kBLd + 2 * h + (j & 1)));  // release: the values above
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(bb.b(kBLd + 2 * h + (j & 1)), (j >> 1) & 1, wd, abort_flag)))
         break;
       // Visible queries of this key: positions >= its own (a suffix of the tile).
       int first = 0, last = static_cast<int>(nq);
       if (!kvalid) first = last;
       else if (p.causal) first = causal_visible(ti.blk, q0, gk - 1, p.L, p.P);
-      if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBS), j & 1, wd, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBH + h), j & 1, wd, abort_flag))) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float sv[32], pv[32];
         tmem_ld32(tS + c * 32, sv);
         tmem_ld32(tP + c * 32, pv);
@@ -484,49 +581,42 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         uint32_t pkp[16], pks[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
-          const int cc = c * 32 + 2 * x;
+          const int lc = c * 32 + 2 * x;  // column within the half
+          const int cc = 64 * h + lc;     // column within the tile
           const bool v0 = cc >= first && cc < last, v1 = cc + 1 >= first && cc + 1 < last;
-          const float p0 = v0 ? ex2(fmaf(sv[2 * x], sl2, -ld[cc])) : 0.f;
-          const float p1 = v1 ? ex2(fmaf(sv[2 * x + 1], sl2, -ld[cc + 1])) : 0.f;
+          const float p0 = v0 ? ex2(fmaf(sv[2 * x], sl2, -ld[lc])) : 0.f;
+          const float p1 = v1 ? ex2(fmaf(sv[2 * x + 1], sl2, -ld[lc + 1])) : 0.f;
           pkp[x] = pack_bf16x2(p0, p1);
-          pks[x] = pack_bf16x2(p0 * (pv[2 * x] - ld[128 + cc]), p1 * (pv[2 * x + 1] - ld[128 + cc + 1]));
+          pks[x] = pack_bf16x2(p0 * (pv[2 * x] - ld[64 + lc]), p1 * (pv[2 * x + 1] - ld[64 + lc + 1]));
         }
         tmem_st16(tS + c * 16, pkp);
         tmem_st16(tP + c * 16, pks);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bb.b(kBP));
+      mbar_arrive(bb.b(kBC + h));
     }
     __syncwarp();
     const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
     if (!aborted) {
       const bool have = j > 0 && __all_sync(0xffffffffu, mbar_wait(bb.b(kBO), 0, wd, abort_flag));
       tc_fence_after();
+      // Warpgroup 0 writes the dV row, warpgroup 1 the dK row.
       const int64_t grow = k_row0 + row;
+      const uint32_t tA = tmem + lane_bits + (h == 0 ? kColAcc0 : kColAcc1);
+      __nv_bfloat16 *dst = (h == 0 ? p.dv : p.dk) + grow * D;
+      const float mul = h == 0 ? 1.f : p.scale;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
         if (have) {
-          tmem_ld32(tV + c * 32, o);
+          tmem_ld32(tA + c * 32, o);
           tmem_wait_ld();
         } else {
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] = 0.f;
         }
-        if (kvalid) store_row_bf16(p.dv + grow * D + c * 32, o, 1.f);
-      }
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        if (have) {
-          tmem_ld32(tK + c * 32, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) o[x] = 0.f;
-        }
-        if (kvalid) store_row_bf16(p.dk + grow * D + c * 32, o, p.scale);
+        if (kvalid) store_row_bf16(dst + c * 32, o, mul);
       }
     }
   }
