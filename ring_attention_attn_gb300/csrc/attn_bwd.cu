@@ -546,23 +546,33 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const bool kvalid = row < nk;
     const int64_t gk = p.causal ? zz_pos(b, min64(k0 + row, p.L - 1), C2, p.P) : 0;
     const float sl2 = p.scale_log2;
+    // LSE (log2 units) and D of this half's 64 queries are staged in SMEM,
+    // double-buffered: thread t < 64 holds the LSE of query t, thread
+    // 64 + t its D, read from global memory one tile ahead.
+    const int qi = row & 63;
+    auto staged = [&](const BIter &t) -> float {
+      const int64_t tq0 = static_cast<int64_t>(t.t) * 128;
+      if (64 * h + qi >= min64(128, p.L - tq0)) return 0.f;
+      const int64_t qrow = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(t.blk) * p.L +
+                           tq0 + 64 * h + qi;
+      return row < 64 ? p.lse[qrow] * kLog2eB : p.Dv[qrow];
+    };
     int j = 0;
-    for (BIter ti = make_iter(); ti.valid(); ++j, ++ti.t, ti.settle()) {
-      // LSE (log2 units) and D of this half's 64 queries, double-buffered.
+    BIter ti = make_iter();
+    float val = ti.valid() ? staged(ti) : 0.f;
+    for (; ti.valid(); ++j) {
+      BIter tn = ti;
+      ++tn.t;
+      tn.settle();
       float *ld = sm_ld + (2 * h + (j & 1)) * 128;
       const int64_t q0 = static_cast<int64_t>(ti.t) * 128;
       const int64_t nq = min64(128, p.L - q0);
-      const int64_t qrow0 =
-          static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(ti.blk) * p.L + q0 + 64 * h;
       // Buffer (h, j&1) was last read two tiles ago; no thread of this
       // warpgroup can still be there, since half h of this tile's S^T needs
       // every one of its arrivals for the previous tile.
-      const int qi = row & 63;
-      if (row < 64)
-        ld[qi] = 64 * h + qi < nq ? p.lse[qrow0 + qi] * kLog2eB : 0.f;
-      else
-        ld[64 + qi] = 64 * h + qi < nq ? p.Dv[qrow0 + qi] : 0.f;
-      mbar_arrive(bb.b(kBLd + 2 * h + (j & 1)));  // release: the values above
+      ld[row < 64 ? qi : 64 + qi] = val;
+      val = tn.valid() ? staged(tn) : 0.f;         // next tile's value, in flight
+      mbar_arrive(bb.b(kBLd + 2 * h + (j & 1)));  // release: the value above
       if (!__all_sync(0xffffffffu,
                       mbar_wait(bb.b(kBLd + 2 * h + (j & 1)), (j >> 1) & 1, wd, abort_flag)))
         break;
@@ -595,6 +605,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bb.b(kBC + h));
+      ti = tn;
     }
     __syncwarp();
     const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
