@@ -52,7 +52,7 @@ struct BCfg {
   static constexpr int kOffKV = 2 * kTile;  // ring of streamed tiles
   static constexpr int kOffBar = kOffKV + kSlots * kTile;
   static constexpr int kBarBytes = 512;
-  static constexpr int kOffLD = kOffBar + kBarBytes;  // [half][buffer](LSE[64], D[64]) fp32
+  static constexpr int kOffLD = kOffBar + kBarBytes;  // [half][buffer](-LSE[64], -D[64]) fp32
   static constexpr int kLDBytes = 2048;
   static constexpr int kSmemBytes = kOffLD + kLDBytes + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -320,6 +320,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const float Drow = valid ? p.Dv[grow] : 0.f;
     const int64_t gq = p.causal ? zz_pos(r, min64(q0 + row, p.L - 1), C2, p.P) : 0;
     const float sl2 = p.scale_log2;
+    const float2 sl2v = make_float2(sl2, sl2), nlse2 = make_float2(-lse2, -lse2),
+                 nD2 = make_float2(-Drow, -Drow);
     int j = 0;
     for (BIter ti = make_iter(); ti.valid(); ++j, ++ti.t, ti.settle()) {
       if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBH + h), j & 1, wd, abort_flag))) break;
@@ -327,6 +329,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const int64_t k0 = static_cast<int64_t>(ti.t) * 128;
       int nvis = static_cast<int>(min64(128, p.L - k0));
       if (p.causal) nvis = causal_visible(ti.blk, k0, gq, p.L, p.P);
+      // Keys [0, nvis) of the tile are visible; when every row of the warp
+      // sees all of this half, no column needs a mask.
+      const bool full = __all_sync(0xffffffffu, nvis >= 64 * h + 64);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         float sv[32], pv[32];
@@ -336,10 +341,15 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
-          const int cc = 64 * h + c * 32 + 2 * x;
-          const float p0 = cc < nvis ? ex2(fmaf(sv[2 * x], sl2, -lse2)) : 0.f;
-          const float p1 = cc + 1 < nvis ? ex2(fmaf(sv[2 * x + 1], sl2, -lse2)) : 0.f;
-          pk[x] = pack_bf16x2(p0 * (pv[2 * x] - Drow), p1 * (pv[2 * x + 1] - Drow));
+          const float2 a = ffma2(make_float2(sv[2 * x], sv[2 * x + 1]), sl2v, nlse2);
+          float2 e = make_float2(ex2(a.x), ex2(a.y));
+          if (!full) {
+            const int cc = 64 * h + c * 32 + 2 * x;
+            e.x = cc < nvis ? e.x : 0.f;
+            e.y = cc + 1 < nvis ? e.y : 0.f;
+          }
+          const float2 ds = fmul2(e, fadd2(make_float2(pv[2 * x], pv[2 * x + 1]), nD2));
+          pk[x] = pack_bf16x2(ds.x, ds.y);
         }
         tmem_st16(tS + c * 16, pk);
       }
@@ -391,7 +401,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const BBars bb = init_bars<D>(sbase);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffBar + kBAbort);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + kBTmemSlot);
-  float *sm_ld = reinterpret_cast<float *>(smem + C::kOffLD);  // [half][buffer](LSE 64 | D 64)
+  float *sm_ld = reinterpret_cast<float *>(smem + C::kOffLD);  // [half][buffer](-LSE 64 | -D 64)
   const Watchdog wd{p.wd.status, p.wd.limit_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -546,16 +556,16 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const bool kvalid = row < nk;
     const int64_t gk = p.causal ? zz_pos(b, min64(k0 + row, p.L - 1), C2, p.P) : 0;
     const float sl2 = p.scale_log2;
-    // LSE (log2 units) and D of this half's 64 queries are staged in SMEM,
-    // double-buffered: thread t < 64 holds the LSE of query t, thread
-    // 64 + t its D, read from global memory one tile ahead.
+    // -LSE (log2 units) and -D of this half's 64 queries are staged in SMEM,
+    // double-buffered: thread t < 64 holds query t's, thread 64 + t its -D,
+    // read from global memory one tile ahead.
     const int qi = row & 63;
     auto staged = [&](const BIter &t) -> float {
       const int64_t tq0 = static_cast<int64_t>(t.t) * 128;
       if (64 * h + qi >= min64(128, p.L - tq0)) return 0.f;
       const int64_t qrow = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(t.blk) * p.L +
                            tq0 + 64 * h + qi;
-      return row < 64 ? p.lse[qrow] * kLog2eB : p.Dv[qrow];
+      return row < 64 ? -(p.lse[qrow] * kLog2eB) : -p.Dv[qrow];
     };
     int j = 0;
     BIter ti = make_iter();
@@ -582,6 +592,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       else if (p.causal) first = causal_visible(ti.blk, q0, gk - 1, p.L, p.P);
       if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBH + h), j & 1, wd, abort_flag))) break;
       tc_fence_after();
+      // When every key row of the warp sees every query of this half, no
+      // column needs a mask.
+      const bool full = __all_sync(0xffffffffu, first <= 64 * h && last >= 64 * h + 64);
+      const float2 sl2v = make_float2(sl2, sl2);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         float sv[32], pv[32];
@@ -590,14 +604,25 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         tmem_wait_ld();
         uint32_t pkp[16], pks[16];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int lc = c * 32 + 2 * x;  // column within the half
-          const int cc = 64 * h + lc;     // column within the tile
-          const bool v0 = cc >= first && cc < last, v1 = cc + 1 >= first && cc + 1 < last;
-          const float p0 = v0 ? ex2(fmaf(sv[2 * x], sl2, -ld[lc])) : 0.f;
-          const float p1 = v1 ? ex2(fmaf(sv[2 * x + 1], sl2, -ld[lc + 1])) : 0.f;
-          pkp[x] = pack_bf16x2(p0, p1);
-          pks[x] = pack_bf16x2(p0 * (pv[2 * x] - ld[64 + lc]), p1 * (pv[2 * x + 1] - ld[64 + lc + 1]));
+        for (int y = 0; y < 8; ++y) {
+          const float4 nl = *reinterpret_cast<const float4 *>(ld + c * 32 + 4 * y);
+          const float4 nd = *reinterpret_cast<const float4 *>(ld + 64 + c * 32 + 4 * y);
+#pragma unroll
+          for (int z = 0; z < 2; ++z) {
+            const int x = 2 * y + z;
+            const float2 a = ffma2(make_float2(sv[2 * x], sv[2 * x + 1]), sl2v,
+                                   z ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y));
+            float2 e = make_float2(ex2(a.x), ex2(a.y));
+            if (!full) {
+              const int cc = 64 * h + c * 32 + 2 * x;  // column within the tile
+              e.x = cc >= first && cc < last ? e.x : 0.f;
+              e.y = cc + 1 >= first && cc + 1 < last ? e.y : 0.f;
+            }
+            const float2 ds = fmul2(e, fadd2(make_float2(pv[2 * x], pv[2 * x + 1]),
+                                             z ? make_float2(nd.z, nd.w) : make_float2(nd.x, nd.y)));
+            pkp[x] = pack_bf16x2(e.x, e.y);
+            pks[x] = pack_bf16x2(ds.x, ds.y);
+          }
         }
         tmem_st16(tS + c * 16, pkp);
         tmem_st16(tP + c * 16, pks);
