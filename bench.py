@@ -295,38 +295,67 @@ def run_ours(a, rank, world, local):
     merge_gbs = merge_bytes / (merge_avg * 1e-3) / 1e9
     peak_t = peaks["bf16_tflops_sustained"]
 
-    # End to end through the public API with host buffers: pinned inputs
-    # copied in and the result copied out inside the timed region.
+    # End to end through the public API with host buffers: every step copies
+    # its inputs in from pinned host memory and its result out to pinned host
+    # memory inside the timed region.  As a serving loop would, the copies run
+    # on their own streams into double-buffered device tensors, so step i+1's
+    # inputs arrive while step i computes and step i's result leaves while
+    # step i+1 computes; the first step's copy-in and the last step's
+    # copy-out are not hidden.
     qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    e2e_steps = max(1, min(a.steps, 5))
+    e2e_steps = max(1, a.steps)
+    ins = [(qd, kd, vd), tuple(torch.empty_like(x) for x in (qd, kd, vd))]
+    outs = [(out, lse), (torch.empty_like(out), torch.empty_like(lse))]
+    hosts = [tuple(torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in o) for o in outs]
+    copy_in = torch.cuda.Stream(dev)
+    copy_out = torch.cuda.Stream(dev)
 
-    def e2e_step():
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        step()
-        oh.copy_(out, non_blocking=True)
-        lh.copy_(lse, non_blocking=True)
+    def e2e_run(nsteps, t0=None, t1=None):
+        ready = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        read = [torch.cuda.Event() for _ in range(2)]
+        if t0 is not None:
+            t0.record(copy_in)
+        for i in range(nsteps):
+            b = i % 2
+            with torch.cuda.stream(copy_in):
+                if i >= 2:
+                    copy_in.wait_event(done[b])  # step i-2 has finished reading ins[b]
+                for dst, src in zip(ins[b], (qh, kh, vh)):
+                    dst.copy_(src, non_blocking=True)
+                ready[b].record(copy_in)
+            stream.wait_event(ready[b])
+            if i >= 2:
+                stream.wait_event(read[b])  # step i-2's result has left outs[b]
+            ra.ring_attn_fwd_rank(*ins[b], w.P, 0, out_fp32=True, out=parts, lse=lparts,
+                                  stream=stream)
+            ra.lse_merge(parts, lparts, out=outs[b][0], lse_out=outs[b][1], stream=stream)
+            done[b].record(stream)
+            with torch.cuda.stream(copy_out):
+                copy_out.wait_event(done[b])
+                for dst, src in zip(hosts[b], outs[b]):
+                    dst.copy_(src, non_blocking=True)
+                read[b].record(copy_out)
+        if t1 is not None:
+            t1.record(copy_out)
 
     if a.no_e2e:
         e2e_steps = 0
     else:
-        e2e_step()
+        e2e_run(2)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    if e2e_steps:
+        e2e_run(e2e_steps, e0, e1)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) if e2e_steps else float("nan")
     if e2e_steps:
         e2e_ms = reduce_max_ms(e2e_ms, dist, dev)
+        if ra.ra_get_status() != 0:
+            raise RuntimeError("device watchdog fired during the end-to-end run")
     e2e_value = (world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12) if e2e_steps else None
     h2d = (q.numel() + k.numel() + v.numel()) * 2
     d2h = out.numel() * 2 + lse.numel() * 4
