@@ -450,27 +450,28 @@ int cp_allgather_attn_fwd(const void *q, const void *k, const void *v, void *out
   void *kg = ws + tb, *vg = ws + 2 * tb;
   cudaError_t e = ra::launch_row_permute(k, kg, BH, S, d * 2, 6, P, H, B, st);
   if (e == cudaSuccess) e = ra::launch_row_permute(v, vg, BH, S, d * 2, 6, P, H, B, st);
-  for (int r = 0; r < P && e == cudaSuccess; ++r) {
-    // Rank r: its own queries (buffer r) against every block of the gathered K/V.
+  if (e == cudaSuccess) {
+    // Every rank's own queries (buffer r) against every block of the gathered
+    // K/V, all ranks in one launch.
     ra::AttnParams p{};
     p.BH = static_cast<int>(BH);
     p.G = 1;
-    p.n_ranks = 1;
+    p.n_ranks = P;
     p.n_stepgroups = 1;
     p.n_pairs = static_cast<int>((L + 255) / 256);
     p.q_rows_bh = L;
+    p.q_rank_stride = BH * L;
     p.kv_rows_bh = S;
     p.L = L;
     p.P = P;
-    p.rank_begin = r;
+    p.rank_begin = 0;
     p.steps_per_group = P;
     p.causal = causal;
     p.scale_log2 = scale_log2(d);
-    p.out = static_cast<uint8_t *>(out) + static_cast<size_t>(r) * BH * L * d * 2;
-    p.lse = lse + static_cast<size_t>(r) * BH * L;
+    p.out = out;
+    p.lse = lse;
     p.wd = wd;
-    const void *qr = static_cast<const uint8_t *>(q) + static_cast<size_t>(r) * BH * L * d * 2;
-    e = ra::launch_ring_attn(qr, BH * L, kg, vg, BH * S, d, false, p, st);
+    e = ra::launch_ring_attn(q, BH * S, kg, vg, BH * S, d, false, p, st);
   }
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }

@@ -121,7 +121,7 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams &p, int u) {
   w.s_lo = p.step_begin + w.part * p.steps_per_group;
   w.s_hi = w.s_lo + p.steps_per_group;
   w.q_row0 = static_cast<int64_t>(w.bh) * p.q_rows_bh + static_cast<int64_t>(w.g) * p.q_rows_g +
-             static_cast<int64_t>(ri) * p.L;
+             static_cast<int64_t>(ri) * (p.q_rank_stride ? p.q_rank_stride : p.L);
   return w;
 }
 

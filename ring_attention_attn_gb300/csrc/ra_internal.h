@@ -23,6 +23,7 @@ struct WatchdogParams {
 struct AttnParams {
   int BH, G, n_ranks, n_stepgroups, n_pairs;
   int64_t q_rows_bh, q_rows_g;    // Q / out / lse row strides (rows)
+  int64_t q_rank_stride;          // rows between consecutive ranks' query chunks (0: L)
   int64_t kv_rows_bh, kv_rows_g;  // K / V row strides (rows)
   int64_t L;                      // rows per ring block (and per rank chunk)
   int P, rank_begin, step_begin, steps_per_group;
