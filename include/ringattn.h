@@ -217,7 +217,11 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
                   void *out_t, float *lse_t, int B, int H, int T, int N, int d, int P,
                   void *workspace, size_t ws_bytes, void *stream);
 
-/* Scratch bytes factored_attn needs for these sizes (0 on bad arguments). */
+/* Scratch bytes factored_attn needs for these sizes (0 on bad arguments):
+ * the temporal output (bf16) and its LSE (fp32) in position-major order and,
+ * when T > 128, room for position-major copies of q, k and v (used when a
+ * rank's chunk of T/P frames is longer than 128; shorter chunks are read in
+ * place). */
 size_t factored_attn_workspace(int B, int H, int T, int N, int d);
 
 /* Size of the fixed device scratch that factored_attn_static works in. */
@@ -232,9 +236,10 @@ size_t factored_attn_workspace(int B, int H, int T, int N, int d);
  * loop in which an allocation (and the synchronisation cudaMalloc implies) is
  * not allowed.
  *  - Limit: the sizes must satisfy factored_attn_workspace(B,H,T,N,d) <=
- *    RA_STATIC_SCRATCH_BYTES (about 65,000 tokens x heads at d = 128,
- *    130,000 at d = 64); larger sizes return RA_ERR_WORKSPACE and launch
- *    nothing.  Other argument errors are those of factored_attn.
+ *    RA_STATIC_SCRATCH_BYTES (for T <= 128 about 258,000 tokens x heads at
+ *    d = 128 and 508,000 at d = 64; for T > 128 about a quarter of that);
+ *    larger sizes return RA_ERR_WORKSPACE and launch nothing.  Other
+ *    argument errors are those of factored_attn.
  *  - The array lives in every GPU that loads the library until the process
  *    exits.  The first call on a device looks up the array's device address
  *    (once per device, with that device current); make that first call before

@@ -579,14 +579,17 @@ int lse_merge(const float *o_parts, const float *lse_parts, int n, int64_t rows,
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
 
-// Workspace of factored_attn: the frame-transposed q, k, v, the temporal
-// output in transposed order (bf16) and its LSE (fp32), each 256-byte aligned.
+// Workspace of factored_attn: the temporal output in position-major order
+// (bf16) and its LSE (fp32), each 256-byte aligned.  A rank chunk of more
+// than 128 frames (possible only when T > 128) is not packed: q, k, v are
+// then first transposed to position-major copies, three more parts.
 static size_t ws_part(size_t bytes) { return (bytes + 255) & ~static_cast<size_t>(255); }
+constexpr int kPackMaxFrames = 128;
 
 size_t factored_attn_workspace(int B, int H, int T, int N, int d) {
   if (B < 0 || H < 0 || T < 0 || N < 0 || check_d(d) != RA_OK) return 0;
   const size_t rows = static_cast<size_t>(B) * H * T * N;
-  return 4 * ws_part(rows * d * 2) + ws_part(rows * 4);
+  return (T > kPackMaxFrames ? 4 : 1) * ws_part(rows * d * 2) + ws_part(rows * 4);
 }
 
 int factored_attn(const void *q, const void *k, const void *v, void *out_s, float *lse_s,
@@ -632,18 +635,28 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
     e = ra::launch_ring_attn(q, BH * S, k, v, BH * S, d, false, p, st);
     if (e != cudaSuccess) return fail_cuda(e);
   }
-  // Temporal: transpose to [N, T] order, then N problems of T tokens per
-  // (b, h), each a ring over P chunks of T/P frames; transpose back.
+  // Temporal: N problems of T tokens per (b, h), each a ring over P chunks
+  // of T/P frames.  Chunks of up to 128 frames are read in place from the
+  // frame-major tensors (packed tiles); longer ones from position-major
+  // copies.  The output is written position-major into the workspace and
+  // transposed back.
+  const bool packed = T / P <= kPackMaxFrames;
   const size_t tbytes = ws_part(static_cast<size_t>(BH * S) * d * 2);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  void *qT = ws, *kT = ws + tbytes, *vT = ws + 2 * tbytes, *oT = ws + 3 * tbytes;
-  float *lT = reinterpret_cast<float *>(ws + 4 * tbytes);
-  const void *src[3] = {q, k, v};
-  void *dst[3] = {qT, kT, vT};
-  for (int i = 0; i < 3; ++i) {
-    e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 2, T, N, 0, st);
-    if (e != cudaSuccess) return fail_cuda(e);
+  const void *tq = q, *tk = k, *tv = v;
+  if (!packed) {
+    void *dst[3] = {ws + tbytes, ws + 2 * tbytes, ws + 3 * tbytes};
+    const void *src[3] = {q, k, v};
+    for (int i = 0; i < 3; ++i) {
+      e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 2, T, N, 0, st);
+      if (e != cudaSuccess) return fail_cuda(e);
+    }
+    tq = dst[0];
+    tk = dst[1];
+    tv = dst[2];
   }
+  void *oT = ws;
+  float *lT = reinterpret_cast<float *>(ws + (packed ? 1 : 4) * tbytes);
   {
     ra::AttnParams p{};
     const int64_t L = T / P;
@@ -657,10 +670,10 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
     p.kv_rows_bh = S;
     p.kv_rows_g = T;
     p.L = L;
-    if (L <= 128) {
+    if (packed) {
       // Short chunks: one 128-row tile carries the same rank's chunk of
-      // floor(128 / L) spatial positions (3-D TMA gather), each position's
-      // queries masked to its own keys.
+      // floor(128 / L) spatial positions (4-D TMA box over the frame-major
+      // tensor), each position's queries masked to its own keys.
       const int pack = static_cast<int>(128 / L) < N ? static_cast<int>(128 / L) : N;
       p.pack = pack;
       p.Lf = static_cast<int>(L);
@@ -679,7 +692,7 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
     p.out = oT;
     p.lse = lT;
     p.wd = wd;
-    e = ra::launch_ring_attn(qT, BH * S, kT, vT, BH * S, d, false, p, st);
+    e = ra::launch_ring_attn(tq, BH * S, tk, tv, BH * S, d, false, p, st);
     if (e != cudaSuccess) return fail_cuda(e);
   }
   e = ra::launch_row_permute(oT, out_t, BH, S, d * 2, 3, T, N, 0, st);

@@ -272,19 +272,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n_loaded > 0 &&
             !mbar_wait(bar0 + 8 * kBarQEmpty, (n_loaded - 1) & 1, wd, abort_flag))
           break;
-        // Packed mode: 3-D box {64 d, Lf rows, pack problems} starting at
-        // the rank's chunk of the unit's first problem.
-        const int32_t pz = static_cast<int32_t>(static_cast<int64_t>(w.bh) * p.pN +
-                                                static_cast<int64_t>(w.g) * p.pack);
+        // Packed mode: box {64 d, Lf frames, pack positions, 1 head} of the
+        // [head][frame][position][d] tensor, starting at the rank's first
+        // frame and the unit's first position.
+        const int32_t pn = w.g * p.pack;
         if (p.pack) {
           mbar_arrive_expect_tx(qfull, g.has_q1 ? 2 * pack_bytes : pack_bytes);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_3d(sbase + C::kOffQ0 + c * C::kChunkBytes, &tm_q, c * 64, w.rank * p.Lf, pz,
-                        qfull);
+            tma_load_4d(sbase + C::kOffQ0 + c * C::kChunkBytes, &tm_q, c * 64, w.rank * p.Lf, pn,
+                        w.bh, qfull);
             if (g.has_q1)
-              tma_load_3d(sbase + C::kOffQ1 + c * C::kChunkBytes, &tm_q, c * 64,
-                          (w.rank + 1) * p.Lf, pz, qfull);
+              tma_load_4d(sbase + C::kOffQ1 + c * C::kChunkBytes, &tm_q, c * 64,
+                          (w.rank + 1) * p.Lf, pn, w.bh, qfull);
           }
         } else {
           const int32_t qy = static_cast<int32_t>(w.q_row0 + g.pair_row0);
@@ -316,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive_expect_tx(kv_full0 + 8 * slot, pack_bytes);
 #pragma unroll
               for (int c = 0; c < C::kChunks; ++c)
-                tma_load_3d(sbase + C::kOffKV + slot * C::kKVTile + c * C::kChunkBytes, map,
-                            c * 64, ti.src * p.Lf, pz, kv_full0 + 8 * slot);
+                tma_load_4d(sbase + C::kOffKV + slot * C::kKVTile + c * C::kChunkBytes, map,
+                            c * 64, ti.src * p.Lf, pn, w.bh, kv_full0 + 8 * slot);
             } else {
               mbar_arrive_expect_tx(kv_full0 + 8 * slot, C::kKVTile);
 #pragma unroll
@@ -704,19 +704,24 @@ cudaError_t make_row_map(CUtensorMap *map, const void *base, int64_t rows, int d
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// 3-D bf16 tensor [problems][rows][d]; box = 64 elements x Lf rows x pack
-// problems, 128-byte swizzle; coordinates past the end read as zero.
-cudaError_t make_pack_map(CUtensorMap *map, const void *base, int64_t problems, int rows, int Lf,
+// Packed temporal problems read in place: the bf16 tensor [BH][T][N][d]
+// (frame-major video tokens) seen as 4-D with dims (d, frame, position,
+// head) and strides (2 B, N·d·2, d·2, T·N·d·2), box = 64 elements x Lf
+// frames x pack positions x 1 head, so a box lands in shared memory
+// position-major (pack problems of Lf rows each).  128-byte swizzle;
+// coordinates past the end read as zero.
+cudaError_t make_pack_map(CUtensorMap *map, const void *base, int64_t BH, int T, int64_t N, int Lf,
                           int pack, int d) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
-                        static_cast<cuuint64_t>(problems)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                           static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(rows)};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(Lf), static_cast<cuuint32_t>(pack)};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+  const cuuint64_t row = static_cast<cuuint64_t>(d) * 2;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(T),
+                        static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[3] = {row * static_cast<cuuint64_t>(N), row,
+                           row * static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(T)};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(Lf), static_cast<cuuint32_t>(pack), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -766,10 +771,9 @@ cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k,
   CUtensorMap mq, mk, mv;
   cudaError_t e;
   if (p.pack) {
-    const int64_t problems = static_cast<int64_t>(p.BH) * p.pN;
-    if ((e = make_pack_map(&mq, q, problems, p.pT, p.Lf, p.pack, d)) != cudaSuccess) return e;
-    if ((e = make_pack_map(&mk, k, problems, p.pT, p.Lf, p.pack, d)) != cudaSuccess) return e;
-    if ((e = make_pack_map(&mv, v, problems, p.pT, p.Lf, p.pack, d)) != cudaSuccess) return e;
+    if ((e = make_pack_map(&mq, q, p.BH, p.pT, p.pN, p.Lf, p.pack, d)) != cudaSuccess) return e;
+    if ((e = make_pack_map(&mk, k, p.BH, p.pT, p.pN, p.Lf, p.pack, d)) != cudaSuccess) return e;
+    if ((e = make_pack_map(&mv, v, p.BH, p.pT, p.pN, p.Lf, p.pack, d)) != cudaSuccess) return e;
   } else {
     if ((e = make_row_map(&mq, q, q_total_rows, d)) != cudaSuccess) return e;
     if ((e = make_row_map(&mk, k, kv_total_rows, d)) != cudaSuccess) return e;

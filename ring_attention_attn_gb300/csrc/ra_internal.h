@@ -34,9 +34,11 @@ struct AttnParams {
   int64_t out_part_stride;        // elements between step groups' outputs
   int64_t lse_part_stride;
   // Packed short problems (temporal factored attention): when pack > 0 the
-  // Q/K/V tensors are [BH * pN problems][pT rows][d] and one tile holds the
-  // rank's chunk (Lf rows) of `pack` consecutive problems: L = pack * Lf,
-  // G = ceil(pN / pack), and a query only sees keys of its own problem.
+  // Q/K/V tensors are frame-major video tokens [BH][pT frames][pN positions]
+  // [d] read in place, each position a problem of pT rows; one tile holds
+  // the rank's chunk (Lf frames) of `pack` consecutive positions:
+  // L = pack * Lf, G = ceil(pN / pack), and a query only sees keys of its
+  // own position.  Outputs are written position-major [BH][pN][pT].
   int pack, Lf, pT;
   int64_t pN;
   // Packed mode only: when pack_ranks > 0 a unit holds the chunks of two

@@ -100,10 +100,12 @@ def test_sizes_beyond_the_addressable_rows_are_rejected():
 
 
 def test_workspace_size():
-    L = _abi.lib()
+    """Temporal output + LSE, position-major; for T > 128 also q, k, v copies."""
+    part = lambda b: (b + 255) // 256 * 256
     rows = 1 * 24 * 48 * 900
-    want = 4 * (((rows * 128 * 2) + 255) // 256 * 256) + ((rows * 4 + 255) // 256 * 256)
-    assert ra.factored_attn_workspace(1, 24, 48, 900, 128) == want
+    assert ra.factored_attn_workspace(1, 24, 48, 900, 128) == part(rows * 256) + part(rows * 4)
+    rows = 2 * 3 * 130 * 7
+    assert ra.factored_attn_workspace(2, 3, 130, 7, 64) == 4 * part(rows * 128) + part(rows * 4)
     assert ra.factored_attn_workspace(1, 24, 48, 900, 96) == 0
 
 

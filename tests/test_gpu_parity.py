@@ -355,7 +355,9 @@ def test_allgather_reducescatter_forms_match_oracle(form, B, H, S, d, P, causal)
 @pytest.mark.parametrize("B,H,T,N,d,P", [(1, 2, 8, 50, 64, 4),    # 2 rank pairs
                                           (1, 2, 12, 50, 64, 3),   # odd P: last rank unpaired
                                           (2, 1, 6, 70, 128, 1),   # one rank
-                                          (1, 3, 24, 40, 128, 2)])
+                                          (1, 3, 24, 40, 128, 2),
+                                          (1, 1, 260, 3, 64, 2),   # 130-frame chunks: not packed
+                                          (1, 2, 130, 4, 128, 1)])
 def test_factored_small_full(B, H, T, N, d, P):
     q, k, v = synth.make_custom((B, H, T * N, d), (B, H, T * N, d), seed=99 + T + P)
     os_, ls, ot, lt = ra.factored_attn(q.cuda(), k.cuda(), v.cuda(), T, N, P)
