@@ -217,11 +217,12 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
                   void *out_t, float *lse_t, int B, int H, int T, int N, int d, int P,
                   void *workspace, size_t ws_bytes, void *stream);
 
-/* Scratch bytes factored_attn needs for these sizes (0 on bad arguments):
- * the temporal output (bf16) and its LSE (fp32) in position-major order and,
- * when T > 128, room for position-major copies of q, k and v (used when a
- * rank's chunk of T/P frames is longer than 128; shorter chunks are read in
- * place). */
+/* Scratch bytes factored_attn needs for these sizes (0 on bad arguments).
+ * 0 when T <= 128: every rank chunk (T/P frames) then fits one 128-row tile
+ * and the temporal pass reads and writes the frame-major tensors in place.
+ * For T > 128, room for position-major copies of q, k, v and of the temporal
+ * output (bf16) and LSE (fp32), used when a chunk is longer than 128 frames.
+ * With a 0 result the workspace pointer may be null. */
 size_t factored_attn_workspace(int B, int H, int T, int N, int d);
 
 /* Size of the fixed device scratch that factored_attn_static works in. */
@@ -236,9 +237,9 @@ size_t factored_attn_workspace(int B, int H, int T, int N, int d);
  * loop in which an allocation (and the synchronisation cudaMalloc implies) is
  * not allowed.
  *  - Limit: the sizes must satisfy factored_attn_workspace(B,H,T,N,d) <=
- *    RA_STATIC_SCRATCH_BYTES (for T <= 128 about 258,000 tokens x heads at
- *    d = 128 and 508,000 at d = 64; for T > 128 about a quarter of that);
- *    larger sizes return RA_ERR_WORKSPACE and launch nothing.  Other
+ *    RA_STATIC_SCRATCH_BYTES: any size with T <= 128 (no scratch needed),
+ *    for T > 128 about 65,000 tokens x heads at d = 128 and 130,000 at
+ *    d = 64; larger sizes return RA_ERR_WORKSPACE and launch nothing.  Other
  *    argument errors are those of factored_attn.
  *  - The array lives in every GPU that loads the library until the process
  *    exits.  The first call on a device looks up the array's device address

@@ -579,17 +579,19 @@ int lse_merge(const float *o_parts, const float *lse_parts, int n, int64_t rows,
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
 
-// Workspace of factored_attn: the temporal output in position-major order
-// (bf16) and its LSE (fp32), each 256-byte aligned.  A rank chunk of more
-// than 128 frames (possible only when T > 128) is not packed: q, k, v are
-// then first transposed to position-major copies, three more parts.
+// Workspace of factored_attn.  Rank chunks of up to 128 frames (always, when
+// T <= 128) are packed: q, k, v are read in place and the temporal output
+// written in place, no workspace.  Longer chunks (possible only when
+// T > 128) run on position-major copies of q, k, v and write a
+// position-major output and LSE that are transposed back: four bf16 parts
+// and one fp32 part, each 256-byte aligned.
 static size_t ws_part(size_t bytes) { return (bytes + 255) & ~static_cast<size_t>(255); }
 constexpr int kPackMaxFrames = 128;
 
 size_t factored_attn_workspace(int B, int H, int T, int N, int d) {
   if (B < 0 || H < 0 || T < 0 || N < 0 || check_d(d) != RA_OK) return 0;
   const size_t rows = static_cast<size_t>(B) * H * T * N;
-  return (T > kPackMaxFrames ? 4 : 1) * ws_part(rows * d * 2) + ws_part(rows * 4);
+  return T > kPackMaxFrames ? 4 * ws_part(rows * d * 2) + ws_part(rows * 4) : 0;
 }
 
 int factored_attn(const void *q, const void *k, const void *v, void *out_s, float *lse_s,
@@ -606,8 +608,10 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
     return RA_ERR_ALIGN;
   if (BH * S > kMaxRows || BH > 0x7fffffff) return RA_ERR_SHAPE;
   const size_t need = factored_attn_workspace(B, H, T, N, d);
-  if (!workspace || ws_bytes < need) return RA_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RA_ERR_ALIGN;
+  if (need > 0) {
+    if (!workspace || ws_bytes < need) return RA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RA_ERR_ALIGN;
+  }
   cudaStream_t st = as_stream(stream);
   ra::WatchdogParams wd;
   if (!watchdog(&wd)) return fail_cuda(cudaGetLastError());
@@ -636,15 +640,19 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
     if (e != cudaSuccess) return fail_cuda(e);
   }
   // Temporal: N problems of T tokens per (b, h), each a ring over P chunks
-  // of T/P frames.  Chunks of up to 128 frames are read in place from the
-  // frame-major tensors (packed tiles); longer ones from position-major
-  // copies.  The output is written position-major into the workspace and
-  // transposed back.
+  // of T/P frames.  Chunks of up to 128 frames are read from and written to
+  // the frame-major tensors in place (packed tiles); longer ones run on
+  // position-major copies whose output is transposed back.
   const bool packed = T / P <= kPackMaxFrames;
-  const size_t tbytes = ws_part(static_cast<size_t>(BH * S) * d * 2);
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
   const void *tq = q, *tk = k, *tv = v;
+  void *oT = out_t;
+  float *lT = lse_t;
   if (!packed) {
+    // Workspace: [output | q | k | v] position-major (bf16), then the LSE.
+    const size_t tbytes = ws_part(static_cast<size_t>(BH * S) * d * 2);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    oT = ws;
+    lT = reinterpret_cast<float *>(ws + 4 * tbytes);
     void *dst[3] = {ws + tbytes, ws + 2 * tbytes, ws + 3 * tbytes};
     const void *src[3] = {q, k, v};
     for (int i = 0; i < 3; ++i) {
@@ -655,8 +663,6 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
     tk = dst[1];
     tv = dst[2];
   }
-  void *oT = ws;
-  float *lT = reinterpret_cast<float *>(ws + (packed ? 1 : 4) * tbytes);
   {
     ra::AttnParams p{};
     const int64_t L = T / P;
@@ -685,6 +691,7 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
       p.n_ranks = (P + 1) / 2;
       p.pack_ranks = P;
       p.n_pairs = 1;
+      p.pack_frame_major = 1;
     }
     p.P = P;
     p.steps_per_group = P;
@@ -695,10 +702,12 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
     e = ra::launch_ring_attn(tq, BH * S, tk, tv, BH * S, d, false, p, st);
     if (e != cudaSuccess) return fail_cuda(e);
   }
-  e = ra::launch_row_permute(oT, out_t, BH, S, d * 2, 3, T, N, 0, st);
-  if (e != cudaSuccess) return fail_cuda(e);
-  e = ra::launch_row_permute(lT, lse_t, BH, S, 4, 3, T, N, 0, st);
-  if (e != cudaSuccess) return fail_cuda(e);
+  if (!packed) {
+    e = ra::launch_row_permute(oT, out_t, BH, S, d * 2, 3, T, N, 0, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+    e = ra::launch_row_permute(lT, lse_t, BH, S, 4, 3, T, N, 0, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
   return RA_OK;
 }
 

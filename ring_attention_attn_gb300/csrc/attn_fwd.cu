@@ -569,11 +569,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const float lse_val = (l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
       const int part = p.part_by_block ? ((w.rank - w.s_lo) % p.P + p.P) % p.P : w.part;
+      // Packed mode: frame f = (w.rank + wg) * Lf + qi % Lf of position
+      // n = g * pack + qi / Lf.
+      const int64_t pf = static_cast<int64_t>(w.rank + wg) * p.Lf + (qi - static_cast<int64_t>(pr) * p.Lf);
+      const int64_t pn = static_cast<int64_t>(w.g) * p.pack + pr;
       const int64_t orow =
-          p.pack ? (static_cast<int64_t>(w.bh) * p.pN + static_cast<int64_t>(w.g) * p.pack + pr) *
-                           p.pT +
-                       static_cast<int64_t>(w.rank + wg) * p.Lf + (qi - static_cast<int64_t>(pr) * p.Lf)
-                 : w.q_row0 + qi;
+          !p.pack                ? w.q_row0 + qi
+          : p.pack_frame_major ? (static_cast<int64_t>(w.bh) * p.pT + pf) * p.pN + pn
+                               : (static_cast<int64_t>(w.bh) * p.pN + pn) * p.pT + pf;
       if (OUT_F32) {
         float *out = reinterpret_cast<float *>(p.out) + part * p.out_part_stride + orow * D;
 #pragma unroll

@@ -38,8 +38,10 @@ struct AttnParams {
   // [d] read in place, each position a problem of pT rows; one tile holds
   // the rank's chunk (Lf frames) of `pack` consecutive positions:
   // L = pack * Lf, G = ceil(pN / pack), and a query only sees keys of its
-  // own position.  Outputs are written position-major [BH][pN][pT].
+  // own position.  Outputs are written position-major [BH][pN][pT], or,
+  // with pack_frame_major, frame-major [BH][pT][pN] like the inputs.
   int pack, Lf, pT;
+  int pack_frame_major;
   int64_t pN;
   // Packed mode only: when pack_ranks > 0 a unit holds the chunks of two
   // consecutive ranks (2 * unit index and the next, below pack_ranks) as its

@@ -78,11 +78,13 @@ def test_argument_errors_are_reported_before_any_launch():
     assert L.ra_cp_shard(good, good, 1, 12, 64, 4, 1, 0, s) == -2
     assert L.ra_cp_shard(good, good, 1, 16, 64, 4, 2, 0, s) == -1
     assert L.ra_frame_transpose(good, odd, 1, 4, 4, 64, 0, s) == -3
-    # factored: T % P, workspace
+    # factored: T % P; workspace too small or missing (chunks over 128 frames)
     assert L.factored_attn(good, good, good, good, good, good, good, 1, 1, 10, 9, 64, 4,
                            good, 1 << 30, s) == -2
-    assert L.factored_attn(good, good, good, good, good, good, good, 1, 1, 8, 9, 64, 4,
+    assert L.factored_attn(good, good, good, good, good, good, good, 1, 1, 136, 9, 64, 1,
                            good, 16, s) == -6
+    assert L.factored_attn(good, good, good, good, good, good, good, 1, 1, 136, 9, 64, 1,
+                           nul, 0, s) == -6
 
 
 def test_sizes_beyond_the_addressable_rows_are_rejected():
@@ -100,10 +102,11 @@ def test_sizes_beyond_the_addressable_rows_are_rejected():
 
 
 def test_workspace_size():
-    """Temporal output + LSE, position-major; for T > 128 also q, k, v copies."""
+    """None for T <= 128 (in place); for T > 128 position-major q, k, v, output
+    (bf16) and LSE (fp32)."""
     part = lambda b: (b + 255) // 256 * 256
-    rows = 1 * 24 * 48 * 900
-    assert ra.factored_attn_workspace(1, 24, 48, 900, 128) == part(rows * 256) + part(rows * 4)
+    assert ra.factored_attn_workspace(1, 24, 48, 900, 128) == 0
+    assert ra.factored_attn_workspace(1, 24, 128, 900, 128) == 0
     rows = 2 * 3 * 130 * 7
     assert ra.factored_attn_workspace(2, 3, 130, 7, 64) == 4 * part(rows * 128) + part(rows * 4)
     assert ra.factored_attn_workspace(1, 24, 48, 900, 96) == 0

@@ -48,7 +48,10 @@ def _max_diff(a, b):
 
 
 @pytest.mark.parametrize("B,H,T,N,d,P,seeds", [(1, 2, 8, 50, 64, 4, (11, 12)),
-                                               (1, 3, 12, 130, 128, 4, (21, 22))])
+                                               (1, 3, 12, 130, 128, 4, (21, 22)),
+                                               # chunks over 128 frames: the scratch is used
+                                               (1, 1, 260, 3, 64, 2, (31, 32)),
+                                               (1, 2, 136, 5, 128, 1, (41, 42))])
 def test_static_scratch_matches_workspace_version_twice(B, H, T, N, d, P, seeds):
     S = T * N
     assert ra.factored_attn_workspace(B, H, T, N, d) <= STATIC_SCRATCH_BYTES
@@ -66,7 +69,7 @@ def test_static_scratch_matches_workspace_version_twice(B, H, T, N, d, P, seeds)
 
 
 def test_static_scratch_refuses_sizes_beyond_its_limit():
-    B, H, T, N, d, P = 1, 24, 48, 900, 128, 4  # needs ~1.07 GB of scratch
+    B, H, T, N, d, P = 1, 24, 256, 900, 128, 1  # 256-frame chunks: ~5.7 GB of scratch
     assert ra.factored_attn_workspace(B, H, T, N, d) > STATIC_SCRATCH_BYTES
     x = torch.empty((1, 1, 1, d), dtype=torch.bfloat16, device="cuda")  # never touched
     lse = torch.empty((1,), dtype=torch.float32, device="cuda")
