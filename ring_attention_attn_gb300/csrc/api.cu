@@ -680,13 +680,17 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
       // Short chunks: one 128-row tile carries the same rank's chunk of
       // floor(128 / L) spatial positions (4-D TMA box over the frame-major
       // tensor), each position's queries masked to its own keys.
-      const int pack = static_cast<int>(128 / L) < N ? static_cast<int>(128 / L) : N;
+      // Chunks of up to 32 frames take 16 or 32 tile rows per position so
+      // that every warp's queries and keys share one 32-column chunk.
+      const int lrow = L <= 16 ? 16 : L <= 32 ? 32 : static_cast<int>(L);
+      const int pack = 128 / lrow < N ? 128 / lrow : N;
       p.pack = pack;
       p.Lf = static_cast<int>(L);
+      p.pLrow = lrow;
       p.pN = N;
       p.pT = T;
       p.G = (N + pack - 1) / pack;
-      p.L = static_cast<int64_t>(pack) * L;
+      p.L = static_cast<int64_t>(pack) * lrow;
       // Two ranks' chunks per CTA (its two query tiles share the key tiles).
       p.n_ranks = (P + 1) / 2;
       p.pack_ranks = P;

@@ -178,12 +178,15 @@ __device__ __forceinline__ UnitGeo unit_geo(const AttnParams &p, int u) {
   return g;
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, int PK>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const AttnParams p, int n_units) {
   using C = Cfg<D>;
+  // PK: 0 = row tiles, 1 = packed short problems, 2 = packed with 16 or 32
+  // rows per problem (warp-packed softmax).
+  constexpr bool kPack = PK != 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -215,11 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (p.pack) {
-    // Rows past pack * Lf of the Q tiles and of every K/V slot are never
+  if (kPack) {
+    // Rows past pack * pLrow of the Q tiles and of every K/V slot are never
     // written by TMA: zero them once so that masked keys meet finite values
     // (P = 0 times V must stay 0).
-    const int r0 = p.pack * p.Lf;
+    const int r0 = p.pack * p.pLrow;
     const int per_chunk = (kBM - r0) * 8;  // 16-byte units
     const int regions = (C::kSlots + 2) * C::kChunks;
     for (int idx = threadIdx.x; idx < regions * per_chunk; idx += kThreads) {
@@ -256,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
       const uint32_t qfull = bar0 + 8 * kBarQFull;
-      const uint32_t pack_bytes = static_cast<uint32_t>(p.pack * p.Lf) * 128u * C::kChunks;
+      const uint32_t pack_bytes = static_cast<uint32_t>(p.pack * p.pLrow) * 128u * C::kChunks;
       const uint64_t keep = l2_policy_evict_last();
       int it = 0;        // K/V slot sequence over all units
       int n_loaded = 0;  // Q pairs loaded
@@ -276,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // [head][frame][position][d] tensor, starting at the rank's first
         // frame and the unit's first position.
         const int32_t pn = w.g * p.pack;
-        if (p.pack) {
+        if (kPack) {
           mbar_arrive_expect_tx(qfull, g.has_q1 ? 2 * pack_bytes : pack_bytes);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c) {
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             const CUtensorMap *map = which ? &tm_v : &tm_k;
-            if (p.pack) {
+            if (kPack) {
               mbar_arrive_expect_tx(kv_full0 + 8 * slot, pack_bytes);
 #pragma unroll
               for (int c = 0; c < C::kChunks; ++c)
@@ -456,12 +459,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(wg == 0 || g.has_q1)) continue;
       // Row within the rank's chunk; in packed mode within the tile, whose
       // rank is w.rank + wg.
-      const int64_t qi = p.pack ? row : g.pair_row0 + wg * kBM + row;
-      // Packed mode: row qi is row qi % Lf of problem g * pack + qi / Lf and
-      // sees only the keys of that problem (columns [lo, lo + Lf) of a tile).
-      const int pr = p.pack ? static_cast<int>(qi / p.Lf) : 0;
+      const int64_t qi = kPack ? row : g.pair_row0 + wg * kBM + row;
+      // Packed mode: row qi is frame qi % pLrow of the chunk of problem
+      // g * pack + qi / pLrow (pLrow >= Lf rows per problem; rows past Lf
+      // hold the next frames and are not written) and sees only the first Lf
+      // keys of that problem (columns [lo, lo + Lf) of a tile).
+      const int pr = kPack ? static_cast<int>(qi / p.pLrow) : 0;
       const bool row_valid =
-          qi < p.L && (!p.pack || static_cast<int64_t>(w.g) * p.pack + pr < p.pN);
+          qi < p.L && (!kPack || (static_cast<int64_t>(w.g) * p.pack + pr < p.pN &&
+                                   qi - static_cast<int64_t>(pr) * p.pLrow < p.Lf));
       const int64_t gq = p.causal ? zz_pos(w.rank, min64(qi, p.L - 1), p.L >> 1, p.P) : 0;
 
       float m_ref = -INFINITY, l = 0.f;
@@ -474,77 +480,142 @@ __global__ void __launch_bounds__(kThreads, 1)
             0xffffffffu, mbar_wait(bar0 + 8 * (kBarSFull + wg), (jt + j) & 1, wd, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        float s[kBN];
+        if constexpr (PK == 2) {
+          float alpha = 1.f;
+          bool rescale = false;
+          float2 rs[4];
 #pragma unroll
-        for (int c = 0; c < kBN / 32; ++c)
-          tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(&s[c * 32]));
-        tmem_wait_ld();
-
-        const int64_t k0 = static_cast<int64_t>(ti.t) * kBN;
-        int nvis = static_cast<int>(min64(kBN, p.L - k0));
-        if (p.causal) nvis = causal_visible(ti.src, k0, gq, p.L, p.P);
-        int lo = 0;
-        if (p.pack) {
-          lo = pr * p.Lf;
-          nvis = min(nvis, lo + p.Lf);
-        }
-        if (lo > 0 || nvis < kBN) {
+          for (int x = 0; x < 4; ++x) rs[x] = make_float2(0.f, 0.f);
+          // Warp-packed temporal tiles: problems of pLrow = 16 or 32 rows sit
+          // at the same offsets in the query and the key tile, so the keys
+          // of this warp's 32 rows are exactly its own 32-column chunk: only
+          // that chunk is loaded and exponentiated, and the other chunks of
+          // P are zero.  A row sees the first Lf columns of its problem.
+          float s[32];
+          tmem_ld32(tS + 32 * quarter, s);
+          tmem_wait_ld();
+          const int lo = p.pLrow == 16 ? (lane & 16) : 0;
+          const int hi = lo + p.Lf;
 #pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (c < lo || c >= nvis) s[c] = -INFINITY;
-        }
-        // Row max with 3-input max (two new scores per instruction), 4 chains.
-        float mx[4];
+          for (int c = 0; c < 32; ++c)
+            if (c < lo || c >= hi) s[c] = -INFINITY;
+          float mx[4];
 #pragma unroll
-        for (int x = 0; x < 4; ++x) mx[x] = fmaxf(s[2 * x], s[2 * x + 1]);
+          for (int x = 0; x < 4; ++x) mx[x] = fmaxf(s[2 * x], s[2 * x + 1]);
 #pragma unroll
-        for (int c = 8; c < kBN; c += 8)
+          for (int c = 8; c < 32; c += 8)
 #pragma unroll
-          for (int x = 0; x < 4; ++x) mx[x] = fmax3(mx[x], s[c + 2 * x], s[c + 2 * x + 1]);
-        const float mxs = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
-        float alpha = 1.f;
-        bool rescale = false;
-        if (mxs > m_ref + kRescaleThreshold) {
-          if (m_ref != -INFINITY) {
-            alpha = ex2(m_ref - mxs);
-            rescale = true;
+            for (int x = 0; x < 4; ++x) mx[x] = fmax3(mx[x], s[c + 2 * x], s[c + 2 * x + 1]);
+          const float mxs = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
+          if (mxs > m_ref + kRescaleThreshold) {
+            if (m_ref != -INFINITY) {
+              alpha = ex2(m_ref - mxs);
+              rescale = true;
+            }
+            m_ref = mxs;
           }
-          m_ref = mxs;
-        }
-        const float shift = (m_ref == -INFINITY) ? 0.f : m_ref;
-        const float2 sl2v = make_float2(sl2, sl2);
-        const float2 nshift = make_float2(-shift, -shift);
-        float2 rs[4];
-#pragma unroll
-        for (int x = 0; x < 4; ++x) rs[x] = make_float2(0.f, 0.f);
-        // P overwrites the first 64 columns of this tile's S (already in
-        // registers): bf16 pairs, lower key in the low half.  Scale/shift and
-        // the row sum use packed f32x2 arithmetic (two scores per instruction).
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t pk[16];
+          const float shift = (m_ref == -INFINITY) ? 0.f : m_ref;
+          const float2 sl2v = make_float2(sl2, sl2);
+          const float2 nshift = make_float2(-shift, -shift);
+          uint32_t pk[16], zero[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
-            const float2 a = ffma2(make_float2(s[32 * c + 2 * x], s[32 * c + 2 * x + 1]), sl2v, nshift);
+            const float2 a = ffma2(make_float2(s[2 * x], s[2 * x + 1]), sl2v, nshift);
             const float2 e = make_float2(ex2(a.x), ex2(a.y));
             rs[x & 3] = fadd2(rs[x & 3], e);
             pk[x] = pack_bf16x2(e.x, e.y);
+            zero[x] = 0u;
           }
-          tmem_st16(tS + c * 16, pk);
-        }
-        const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
-        const float2 r = fadd2(r01, r23);
-        const float rsum = r.x + r.y;
-        l = l * alpha + rsum;
-        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_wait_ld();
+          for (int c = 0; c < kBN / 32; ++c) tmem_st16(tS + c * 16, c == quarter ? pk : zero);
+          const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
+          const float2 r = fadd2(r01, r23);
+          const float rsum = r.x + r.y;
+          l = l * alpha + rsum;
+          if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] *= alpha;
-            tmem_st32(tO + c * 32, o);
+            for (int c = 0; c < D / 32; ++c) {
+              float o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) o[x] *= alpha;
+              tmem_st32(tO + c * 32, o);
+            }
+          }
+        } else {
+          float s[kBN];
+#pragma unroll
+          for (int c = 0; c < kBN / 32; ++c)
+            tmem_ld32(tS + c * 32, *reinterpret_cast<float(*)[32]>(&s[c * 32]));
+          tmem_wait_ld();
+
+          const int64_t k0 = static_cast<int64_t>(ti.t) * kBN;
+          int nvis = static_cast<int>(min64(kBN, p.L - k0));
+          if (p.causal) nvis = causal_visible(ti.src, k0, gq, p.L, p.P);
+          int lo = 0;
+          if (kPack) {
+            lo = pr * p.pLrow;
+            nvis = min(nvis, lo + p.Lf);
+          }
+          if (lo > 0 || nvis < kBN) {
+#pragma unroll
+            for (int c = 0; c < kBN; ++c)
+              if (c < lo || c >= nvis) s[c] = -INFINITY;
+          }
+          // Row max with 3-input max (two new scores per instruction), 4 chains.
+          float mx[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) mx[x] = fmaxf(s[2 * x], s[2 * x + 1]);
+#pragma unroll
+          for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) mx[x] = fmax3(mx[x], s[c + 2 * x], s[c + 2 * x + 1]);
+          const float mxs = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
+          float alpha = 1.f;
+          bool rescale = false;
+          if (mxs > m_ref + kRescaleThreshold) {
+            if (m_ref != -INFINITY) {
+              alpha = ex2(m_ref - mxs);
+              rescale = true;
+            }
+            m_ref = mxs;
+          }
+          const float shift = (m_ref == -INFINITY) ? 0.f : m_ref;
+          const float2 sl2v = make_float2(sl2, sl2);
+          const float2 nshift = make_float2(-shift, -shift);
+          float2 rs[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) rs[x] = make_float2(0.f, 0.f);
+          // P overwrites the first 64 columns of this tile's S (already in
+          // registers): bf16 pairs, lower key in the low half.  Scale/shift and
+          // the row sum use packed f32x2 arithmetic (two scores per instruction).
+#pragma unroll
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              const float2 a = ffma2(make_float2(s[32 * c + 2 * x], s[32 * c + 2 * x + 1]), sl2v, nshift);
+              const float2 e = make_float2(ex2(a.x), ex2(a.y));
+              rs[x & 3] = fadd2(rs[x & 3], e);
+              pk[x] = pack_bf16x2(e.x, e.y);
+            }
+            tmem_st16(tS + c * 16, pk);
+          }
+          const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
+          const float2 r = fadd2(r01, r23);
+          const float rsum = r.x + r.y;
+          l = l * alpha + rsum;
+          if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              float o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) o[x] *= alpha;
+              tmem_st32(tO + c * 32, o);
+            }
           }
         }
         tmem_wait_st();
@@ -569,12 +640,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       const float lse_val = (l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
       const int part = p.part_by_block ? ((w.rank - w.s_lo) % p.P + p.P) % p.P : w.part;
-      // Packed mode: frame f = (w.rank + wg) * Lf + qi % Lf of position
-      // n = g * pack + qi / Lf.
-      const int64_t pf = static_cast<int64_t>(w.rank + wg) * p.Lf + (qi - static_cast<int64_t>(pr) * p.Lf);
+      // Packed mode: frame f = (w.rank + wg) * Lf + qi % pLrow of position
+      // n = g * pack + qi / pLrow.
+      const int64_t pf = static_cast<int64_t>(w.rank + wg) * p.Lf + (qi - static_cast<int64_t>(pr) * p.pLrow);
       const int64_t pn = static_cast<int64_t>(w.g) * p.pack + pr;
       const int64_t orow =
-          !p.pack                ? w.q_row0 + qi
+          !kPack                 ? w.q_row0 + qi
           : p.pack_frame_major ? (static_cast<int64_t>(w.bh) * p.pT + pf) * p.pN + pn
                                : (static_cast<int64_t>(w.bh) * p.pN + pn) * p.pT + pf;
       if (OUT_F32) {
@@ -709,11 +780,11 @@ cudaError_t make_row_map(CUtensorMap *map, const void *base, int64_t rows, int d
 
 // Packed temporal problems read in place: the bf16 tensor [BH][T][N][d]
 // (frame-major video tokens) seen as 4-D with dims (d, frame, position,
-// head) and strides (2 B, N·d·2, d·2, T·N·d·2), box = 64 elements x Lf
+// head) and strides (2 B, N·d·2, d·2, T·N·d·2), box = 64 elements x Lrow
 // frames x pack positions x 1 head, so a box lands in shared memory
-// position-major (pack problems of Lf rows each).  128-byte swizzle;
+// position-major (pack problems of Lrow rows each).  128-byte swizzle;
 // coordinates past the end read as zero.
-cudaError_t make_pack_map(CUtensorMap *map, const void *base, int64_t BH, int T, int64_t N, int Lf,
+cudaError_t make_pack_map(CUtensorMap *map, const void *base, int64_t BH, int T, int64_t N, int Lrow,
                           int pack, int d) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
@@ -722,7 +793,7 @@ cudaError_t make_pack_map(CUtensorMap *map, const void *base, int64_t BH, int T,
                         static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[3] = {row * static_cast<cuuint64_t>(N), row,
                            row * static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(T)};
-  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(Lf), static_cast<cuuint32_t>(pack), 1};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(Lrow), static_cast<cuuint32_t>(pack), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -730,7 +801,7 @@ cudaError_t make_pack_map(CUtensorMap *map, const void *base, int64_t BH, int T,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, int PK>
 cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                            const AttnParams &p, int64_t n_units, cudaStream_t stream) {
   using C = Cfg<D>;
@@ -740,7 +811,7 @@ cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const C
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(ring_attn_kernel<D, OUT_F32>,
+    e = cudaFuncSetAttribute(ring_attn_kernel<D, OUT_F32, PK>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -758,8 +829,9 @@ cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const C
   const int64_t tiles_per_unit = ((p.L + kBN - 1) / kBN) * p.steps_per_group;
   const int64_t grid =
       (tiles_per_unit <= kPersistMaxTiles && n_units > sms[dev]) ? sms[dev] : n_units;
-  ring_attn_kernel<D, OUT_F32><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
-      mq, mk, mv, p, static_cast<int>(n_units));
+  ring_attn_kernel<D, OUT_F32, PK>
+      <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p,
+                                                                          static_cast<int>(n_units));
   return cudaGetLastError();
 }
 
@@ -774,19 +846,28 @@ cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k,
   CUtensorMap mq, mk, mv;
   cudaError_t e;
   if (p.pack) {
-    if ((e = make_pack_map(&mq, q, p.BH, p.pT, p.pN, p.Lf, p.pack, d)) != cudaSuccess) return e;
-    if ((e = make_pack_map(&mk, k, p.BH, p.pT, p.pN, p.Lf, p.pack, d)) != cudaSuccess) return e;
-    if ((e = make_pack_map(&mv, v, p.BH, p.pT, p.pN, p.Lf, p.pack, d)) != cudaSuccess) return e;
+    if (out_f32 || p.pLrow < p.Lf || p.pack * p.pLrow > kBM) return cudaErrorInvalidValue;
+    if ((e = make_pack_map(&mq, q, p.BH, p.pT, p.pN, p.pLrow, p.pack, d)) != cudaSuccess) return e;
+    if ((e = make_pack_map(&mk, k, p.BH, p.pT, p.pN, p.pLrow, p.pack, d)) != cudaSuccess) return e;
+    if ((e = make_pack_map(&mv, v, p.BH, p.pT, p.pN, p.pLrow, p.pack, d)) != cudaSuccess) return e;
+    // Problems of 16 or 32 rows: every warp's rows and keys share one
+    // 32-column chunk (the warp-packed softmax).
+    const bool wp = p.pLrow == 16 || p.pLrow == 32;
+    if (d == 128)
+      return wp ? launch_variant<128, false, 2>(mq, mk, mv, p, n_units, stream)
+                : launch_variant<128, false, 1>(mq, mk, mv, p, n_units, stream);
+    return wp ? launch_variant<64, false, 2>(mq, mk, mv, p, n_units, stream)
+              : launch_variant<64, false, 1>(mq, mk, mv, p, n_units, stream);
   } else {
     if ((e = make_row_map(&mq, q, q_total_rows, d)) != cudaSuccess) return e;
     if ((e = make_row_map(&mk, k, kv_total_rows, d)) != cudaSuccess) return e;
     if ((e = make_row_map(&mv, v, kv_total_rows, d)) != cudaSuccess) return e;
   }
   if (d == 128)
-    return out_f32 ? launch_variant<128, true>(mq, mk, mv, p, n_units, stream)
-                   : launch_variant<128, false>(mq, mk, mv, p, n_units, stream);
-  return out_f32 ? launch_variant<64, true>(mq, mk, mv, p, n_units, stream)
-                 : launch_variant<64, false>(mq, mk, mv, p, n_units, stream);
+    return out_f32 ? launch_variant<128, true, 0>(mq, mk, mv, p, n_units, stream)
+                   : launch_variant<128, false, 0>(mq, mk, mv, p, n_units, stream);
+  return out_f32 ? launch_variant<64, true, 0>(mq, mk, mv, p, n_units, stream)
+                 : launch_variant<64, false, 0>(mq, mk, mv, p, n_units, stream);
 }
 
 cudaError_t launch_watchdog_selftest(const WatchdogParams &wd, cudaStream_t stream) {

@@ -41,6 +41,7 @@ struct AttnParams {
   // own position.  Outputs are written position-major [BH][pN][pT], or,
   // with pack_frame_major, frame-major [BH][pT][pN] like the inputs.
   int pack, Lf, pT;
+  int pLrow;  // tile rows per problem, >= Lf (16 or 32 for the warp-packed softmax)
   int pack_frame_major;
   int64_t pN;
   // Packed mode only: when pack_ranks > 0 a unit holds the chunks of two

@@ -356,6 +356,8 @@ def test_allgather_reducescatter_forms_match_oracle(form, B, H, S, d, P, causal)
                                           (1, 2, 12, 50, 64, 3),   # odd P: last rank unpaired
                                           (2, 1, 6, 70, 128, 1),   # one rank
                                           (1, 3, 24, 40, 128, 2),
+                                          (1, 2, 40, 9, 64, 2),    # 20-frame chunks: 32 rows each
+                                          (1, 1, 48, 5, 128, 1),   # 48-frame chunks: 2 per tile
                                           (1, 1, 260, 3, 64, 2),   # 130-frame chunks: not packed
                                           (1, 2, 130, 4, 128, 1)])
 def test_factored_small_full(B, H, T, N, d, P):
