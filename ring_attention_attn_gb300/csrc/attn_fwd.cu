@@ -136,6 +136,7 @@ struct TileIter {
     t = 0;
     src = ((w.rank - s) % p.P + p.P) % p.P;
   }
+  template <bool CAUSAL>
   __device__ __forceinline__ void settle(const AttnParams &p, const Unit &w, int n_t,
                                          int64_t gq_max) {
     while (s < w.s_hi) {
@@ -145,7 +146,7 @@ struct TileIter {
         src = (src == 0) ? p.P - 1 : src - 1;  // next block in ring order
         continue;
       }
-      if (p.causal) {
+      if (CAUSAL) {
         const int64_t gk_min = zz_pos(src, static_cast<int64_t>(t) * kBN, p.L >> 1, p.P);
         if (gk_min > gq_max) {
           ++t;
@@ -166,6 +167,7 @@ struct UnitGeo {
   bool has_q1;
 };
 
+template <bool CAUSAL>
 __device__ __forceinline__ UnitGeo unit_geo(const AttnParams &p, int u) {
   UnitGeo g;
   g.w = decode_unit(p, u);
@@ -173,12 +175,12 @@ __device__ __forceinline__ UnitGeo unit_geo(const AttnParams &p, int u) {
   // Packed mode pairs rank chunks: tile 1 is the next rank's chunk.
   g.has_q1 = p.pack ? (p.pack_ranks > 0 && g.w.rank + 1 < p.rank_begin + p.pack_ranks)
                     : g.pair_row0 + kBM < p.L;
-  g.gq_max = p.causal ? zz_pos(g.w.rank, min64(g.pair_row0 + 2 * kBM - 1, p.L - 1), p.L >> 1, p.P)
+  g.gq_max = CAUSAL ? zz_pos(g.w.rank, min64(g.pair_row0 + 2 * kBM - 1, p.L - 1), p.L >> 1, p.P)
                       : 0;
   return g;
 }
 
-template <int D, bool OUT_F32, int PK>
+template <int D, bool OUT_F32, int PK, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -265,11 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int n_loaded = 0;  // Q pairs loaded
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const UnitGeo g = unit_geo(p, u);
+        const UnitGeo g = unit_geo<CAUSAL>(p, u);
         const Unit &w = g.w;
         TileIter ti;
         ti.init(p, w);
-        ti.settle(p, w, n_t, g.gq_max);
+        ti.settle<CAUSAL>(p, w, n_t, g.gq_max);
         if (!ti.valid(w)) continue;
         // The previous pair's last QK^T must have read the Q buffers.
         if (n_loaded > 0 &&
@@ -331,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++it;
           }
           ++ti.t;
-          ti.settle(p, w, n_t, g.gq_max);
+          ti.settle<CAUSAL>(p, w, n_t, g.gq_max);
         }
       }
       // Drain: every copy issued must land before the CTA may exit.
@@ -362,13 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int jt[2] = {0, 0};  // tiles handed to each softmax warpgroup so far
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const UnitGeo g = unit_geo(p, u);
+        const UnitGeo g = unit_geo<CAUSAL>(p, u);
         const Unit &w = g.w;
         const bool has_q1 = g.has_q1;
         const int nq = has_q1 ? 2 : 1;
         TileIter ti;
         ti.init(p, w);
-        ti.settle(p, w, n_t, g.gq_max);
+        ti.settle<CAUSAL>(p, w, n_t, g.gq_max);
         if (!ti.valid(w)) continue;
         if (!(ok = mbar_wait(bar0 + 8 * kBarQFull, n_loaded & 1, wd, abort_flag))) break;
         ++n_loaded;
@@ -388,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (;; ++j) {
           const int v_it = it;
           ++ti.t;
-          ti.settle(p, w, n_t, g.gq_max);
+          ti.settle<CAUSAL>(p, w, n_t, g.gq_max);
           const bool more = ti.valid(w);
           // The pair's last QK^T has been issued: the Q buffers are free once
           // it completes.
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int jt = 0;      // tiles of this warpgroup so far (S_full / P_full phases)
     int n_done = 0;  // units whose O this warpgroup has read (O_done phases)
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const UnitGeo g = unit_geo(p, u);
+      const UnitGeo g = unit_geo<CAUSAL>(p, u);
       const Unit &w = g.w;
       if (!(wg == 0 || g.has_q1)) continue;
       // Row within the rank's chunk; in packed mode within the tile, whose
@@ -468,13 +470,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_valid =
           qi < p.L && (!kPack || (static_cast<int64_t>(w.g) * p.pack + pr < p.pN &&
                                    qi - static_cast<int64_t>(pr) * p.pLrow < p.Lf));
-      const int64_t gq = p.causal ? zz_pos(w.rank, min64(qi, p.L - 1), p.L >> 1, p.P) : 0;
+      const int64_t gq = CAUSAL ? zz_pos(w.rank, min64(qi, p.L - 1), p.L >> 1, p.P) : 0;
 
       float m_ref = -INFINITY, l = 0.f;
       int j = 0;
       TileIter ti;
       ti.init(p, w);
-      ti.settle(p, w, n_t, g.gq_max);
+      ti.settle<CAUSAL>(p, w, n_t, g.gq_max);
       while (ti.valid(w)) {
         const bool ok = __all_sync(
             0xffffffffu, mbar_wait(bar0 + 8 * (kBarSFull + wg), (jt + j) & 1, wd, abort_flag));
@@ -552,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
           const int64_t k0 = static_cast<int64_t>(ti.t) * kBN;
           int nvis = static_cast<int>(min64(kBN, p.L - k0));
-          if (p.causal) nvis = causal_visible(ti.src, k0, gq, p.L, p.P);
+          if (CAUSAL) nvis = causal_visible(ti.src, k0, gq, p.L, p.P);
           int lo = 0;
           if (kPack) {
             lo = pr * p.pLrow;
@@ -623,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar0 + 8 * (kBarPFull + wg));
         ++j;
         ++ti.t;
-        ti.settle(p, w, n_t, g.gq_max);
+        ti.settle<CAUSAL>(p, w, n_t, g.gq_max);
       }
       __syncwarp();
       const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
@@ -801,7 +803,7 @@ cudaError_t make_pack_map(CUtensorMap *map, const void *base, int64_t BH, int T,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, bool OUT_F32, int PK>
+template <int D, bool OUT_F32, int PK, bool CAUSAL>
 cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                            const AttnParams &p, int64_t n_units, cudaStream_t stream) {
   using C = Cfg<D>;
@@ -811,7 +813,7 @@ cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const C
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(ring_attn_kernel<D, OUT_F32, PK>,
+    e = cudaFuncSetAttribute(ring_attn_kernel<D, OUT_F32, PK, CAUSAL>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -829,7 +831,7 @@ cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const C
   const int64_t tiles_per_unit = ((p.L + kBN - 1) / kBN) * p.steps_per_group;
   const int64_t grid =
       (tiles_per_unit <= kPersistMaxTiles && n_units > sms[dev]) ? sms[dev] : n_units;
-  ring_attn_kernel<D, OUT_F32, PK>
+  ring_attn_kernel<D, OUT_F32, PK, CAUSAL>
       <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p,
                                                                           static_cast<int>(n_units));
   return cudaGetLastError();
@@ -846,7 +848,8 @@ cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k,
   CUtensorMap mq, mk, mv;
   cudaError_t e;
   if (p.pack) {
-    if (out_f32 || p.pLrow < p.Lf || p.pack * p.pLrow > kBM) return cudaErrorInvalidValue;
+    if (out_f32 || p.causal || p.pLrow < p.Lf || p.pack * p.pLrow > kBM)
+      return cudaErrorInvalidValue;
     if ((e = make_pack_map(&mq, q, p.BH, p.pT, p.pN, p.pLrow, p.pack, d)) != cudaSuccess) return e;
     if ((e = make_pack_map(&mk, k, p.BH, p.pT, p.pN, p.pLrow, p.pack, d)) != cudaSuccess) return e;
     if ((e = make_pack_map(&mv, v, p.BH, p.pT, p.pN, p.pLrow, p.pack, d)) != cudaSuccess) return e;
@@ -854,20 +857,29 @@ cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k,
     // 32-column chunk (the warp-packed softmax).
     const bool wp = p.pLrow == 16 || p.pLrow == 32;
     if (d == 128)
-      return wp ? launch_variant<128, false, 2>(mq, mk, mv, p, n_units, stream)
-                : launch_variant<128, false, 1>(mq, mk, mv, p, n_units, stream);
-    return wp ? launch_variant<64, false, 2>(mq, mk, mv, p, n_units, stream)
-              : launch_variant<64, false, 1>(mq, mk, mv, p, n_units, stream);
+      return wp ? launch_variant<128, false, 2, false>(mq, mk, mv, p, n_units, stream)
+                : launch_variant<128, false, 1, false>(mq, mk, mv, p, n_units, stream);
+    return wp ? launch_variant<64, false, 2, false>(mq, mk, mv, p, n_units, stream)
+              : launch_variant<64, false, 1, false>(mq, mk, mv, p, n_units, stream);
   } else {
     if ((e = make_row_map(&mq, q, q_total_rows, d)) != cudaSuccess) return e;
     if ((e = make_row_map(&mk, k, kv_total_rows, d)) != cudaSuccess) return e;
     if ((e = make_row_map(&mv, v, kv_total_rows, d)) != cudaSuccess) return e;
   }
-  if (d == 128)
-    return out_f32 ? launch_variant<128, true, 0>(mq, mk, mv, p, n_units, stream)
-                   : launch_variant<128, false, 0>(mq, mk, mv, p, n_units, stream);
-  return out_f32 ? launch_variant<64, true, 0>(mq, mk, mv, p, n_units, stream)
-                 : launch_variant<64, false, 0>(mq, mk, mv, p, n_units, stream);
+  // Row tiles: the causal mask and the tile skipping it allows are compiled
+  // only into the causal instantiations.
+  if (d == 128) {
+    if (p.causal)
+      return out_f32 ? launch_variant<128, true, 0, true>(mq, mk, mv, p, n_units, stream)
+                     : launch_variant<128, false, 0, true>(mq, mk, mv, p, n_units, stream);
+    return out_f32 ? launch_variant<128, true, 0, false>(mq, mk, mv, p, n_units, stream)
+                   : launch_variant<128, false, 0, false>(mq, mk, mv, p, n_units, stream);
+  }
+  if (p.causal)
+    return out_f32 ? launch_variant<64, true, 0, true>(mq, mk, mv, p, n_units, stream)
+                   : launch_variant<64, false, 0, true>(mq, mk, mv, p, n_units, stream);
+  return out_f32 ? launch_variant<64, true, 0, false>(mq, mk, mv, p, n_units, stream)
+                 : launch_variant<64, false, 0, false>(mq, mk, mv, p, n_units, stream);
 }
 
 cudaError_t launch_watchdog_selftest(const WatchdogParams &wd, cudaStream_t stream) {
