@@ -64,29 +64,31 @@ __device__ __forceinline__ uint32_t global_source_row(const PermuteArgs &p, uint
   return ((R * B + b) * Hp + (h - R * Hp)) * S + r * L + i;
 }
 
-// Source row (within one (b,h) slice) of output row o.
-__device__ __forceinline__ int64_t source_row(const PermuteArgs &p, int64_t o) {
+// Source row (within one (b,h) slice) of output row o; 32-bit arithmetic
+// (rows are below 2^31).
+__device__ __forceinline__ uint32_t source_row(const PermuteArgs &p, uint32_t o) {
+  const uint32_t S = static_cast<uint32_t>(p.S);
   switch (p.mode) {
     case 0: {  // y[j] = x[s2g(j)]
       if (p.layout == 0) return o;
-      const int64_t P = p.a, L = p.S / P, C = L >> 1;
-      const int64_t r = o / L, i = o - r * L;
+      const uint32_t P = static_cast<uint32_t>(p.a), L = S / P, C = L >> 1;
+      const uint32_t r = o / L, i = o - r * L;
       return i < C ? r * C + i : (2 * P - 1 - r) * C + (i - C);
     }
     case 1: {  // y[g] = x[g2s(g)]
       if (p.layout == 0) return o;
-      const int64_t P = p.a, L = p.S / P, C = L >> 1;
-      const int64_t chunk = o / C, off = o - chunk * C;
+      const uint32_t P = static_cast<uint32_t>(p.a), L = S / P, C = L >> 1;
+      const uint32_t chunk = o / C, off = o - chunk * C;
       return chunk < P ? chunk * L + off : (2 * P - 1 - chunk) * L + C + off;
     }
     case 2: {  // output [N, T]: row n*T + t <- input row t*N + n
-      const int64_t T = p.a, N = p.b;
-      const int64_t n = o / T, t = o - n * T;
+      const uint32_t T = static_cast<uint32_t>(p.a), N = static_cast<uint32_t>(p.b);
+      const uint32_t n = o / T, t = o - n * T;
       return t * N + n;
     }
     default: {  // output [T, N]: row t*N + n <- input row n*T + t
-      const int64_t T = p.a, N = p.b;
-      const int64_t t = o / N, n = o - t * N;
+      const uint32_t T = static_cast<uint32_t>(p.a), N = static_cast<uint32_t>(p.b);
+      const uint32_t t = o / N, n = o - t * N;
       return n * T + t;
     }
   }
@@ -114,8 +116,9 @@ __global__ void __launch_bounds__(256) row_permute_kernel(const Vec *__restrict_
         if (p.mode >= 4) {
           src = global_source_row(p, static_cast<uint32_t>(row));
         } else {
-          const int64_t bh = row / p.S, o = row - bh * p.S;
-          src = bh * p.S + source_row(p, o);
+          const uint32_t S = static_cast<uint32_t>(p.S), r32 = static_cast<uint32_t>(row);
+          const uint32_t bh = r32 / S, o = r32 - bh * S;
+          src = static_cast<int64_t>(bh * S + source_row(p, o));
         }
         v[u] = x[src * PIECES + piece];
         dst[u] = e;
