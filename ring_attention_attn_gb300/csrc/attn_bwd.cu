@@ -87,9 +87,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
 
 // K/V blocks for rank r (dQ) or query chunks for block b (dK/dV), in ring
 // order, in 128-row tiles; causal tiles with nothing visible are skipped.
+template <bool CAUSAL>
 struct BIter {
   int s, t, blk;
-  int P, n_t, causal, dir;  // dir -1: blk = (r - s) mod P; +1: blk = (b + s) mod P
+  int P, n_t, dir;  // dir -1: blk = (r - s) mod P; +1: blk = (b + s) mod P
   int64_t C, limit;         // causal: dQ skips tiles with min position > limit,
                             //         dK/dV skips tiles with max position < limit
   int64_t L;
@@ -101,7 +102,7 @@ struct BIter {
         blk = dir < 0 ? (blk == 0 ? P - 1 : blk - 1) : (blk == P - 1 ? 0 : blk + 1);
         continue;
       }
-      if (causal) {
+      if (CAUSAL) {
         const int64_t t0 = static_cast<int64_t>(t) * 128;
         const bool skip = dir < 0 ? zz_pos(blk, t0, C, P) > limit
                                   : zz_pos(blk, min64(t0 + 127, L - 1), C, P) < limit;
@@ -156,7 +157,7 @@ __device__ __forceinline__ void issue_acc_k64(uint32_t d_tmem, uint32_t a_tmem, 
 constexpr uint64_t kHalfRows = (64 * 128) >> 4;
 
 // ------------------------------------------------------------------ dQ ----
-template <int D>
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreadsB, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -181,9 +182,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const int64_t q0 = static_cast<int64_t>(qt) * 128;
   const int64_t nq = min64(128, p.L - q0);
   const int64_t q_row0 = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(r) * p.L + q0;
-  const int64_t gq_max = p.causal ? zz_pos(r, q0 + nq - 1, C2, p.P) : 0;
+  const int64_t gq_max = CAUSAL ? zz_pos(r, q0 + nq - 1, C2, p.P) : 0;
   auto make_iter = [&]() {
-    BIter it{0, 0, r, p.P, p.n_t, p.causal, -1, C2, gq_max, p.L};
+    BIter<CAUSAL> it{0, 0, r, p.P, p.n_t, -1, C2, gq_max, p.L};
     it.settle();
     return it;
   };
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       int it = 0;
       bool ok = true;
-      for (BIter ti = make_iter(); ok && ti.valid(); ++ti.t, ti.settle()) {
+      for (auto ti = make_iter(); ok && ti.valid(); ++ti.t, ti.settle()) {
         const int32_t ky = static_cast<int32_t>(static_cast<int64_t>(bh) * p.S +
                                                 static_cast<int64_t>(ti.blk) * p.L +
                                                 static_cast<int64_t>(ti.t) * 128);
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       mma_commit_e(bb.b(kBH + h));
     };
     bool issued = false, ok = true;
-    BIter ti = make_iter();
+    auto ti = make_iter();
     if (ti.valid() && mbar_wait(bb.b(kBA), 0, wd, abort_flag)) {
       tc_fence_after();
       int it = 0;  // K_j in slot it, V_j in it + 1
@@ -318,17 +319,17 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const int64_t grow = q_row0 + row;
     const float lse2 = valid ? p.lse[grow] * kLog2eB : 0.f;
     const float Drow = valid ? p.Dv[grow] : 0.f;
-    const int64_t gq = p.causal ? zz_pos(r, min64(q0 + row, p.L - 1), C2, p.P) : 0;
+    const int64_t gq = CAUSAL ? zz_pos(r, min64(q0 + row, p.L - 1), C2, p.P) : 0;
     const float sl2 = p.scale_log2;
     const float2 sl2v = make_float2(sl2, sl2), nlse2 = make_float2(-lse2, -lse2),
                  nD2 = make_float2(-Drow, -Drow);
     int j = 0;
-    for (BIter ti = make_iter(); ti.valid(); ++j, ++ti.t, ti.settle()) {
+    for (auto ti = make_iter(); ti.valid(); ++j, ++ti.t, ti.settle()) {
       if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBH + h), j & 1, wd, abort_flag))) break;
       tc_fence_after();
       const int64_t k0 = static_cast<int64_t>(ti.t) * 128;
       int nvis = static_cast<int>(min64(128, p.L - k0));
-      if (p.causal) nvis = causal_visible(ti.blk, k0, gq, p.L, p.P);
+      if (CAUSAL) nvis = causal_visible(ti.blk, k0, gq, p.L, p.P);
       // Keys [0, nvis) of the tile are visible; when every row of the warp
       // sees all of this half, no column needs a mask.
       const bool full = __all_sync(0xffffffffu, nvis >= 64 * h + 64);
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 }
 
 // ---------------------------------------------------------------- dK/dV ----
-template <int D>
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreadsB, 1)
     bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -414,9 +415,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const int64_t k0 = static_cast<int64_t>(kt) * 128;
   const int64_t nk = min64(128, p.L - k0);
   const int64_t k_row0 = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(b) * p.L + k0;
-  const int64_t gk_min = p.causal ? zz_pos(b, k0, C2, p.P) : 0;
+  const int64_t gk_min = CAUSAL ? zz_pos(b, k0, C2, p.P) : 0;
   auto make_iter = [&]() {
-    BIter it{0, 0, b, p.P, p.n_t, p.causal, +1, C2, gk_min, p.L};
+    BIter<CAUSAL> it{0, 0, b, p.P, p.n_t, +1, C2, gk_min, p.L};
     it.settle();
     return it;
   };
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       int it = 0;
       bool ok = true;
-      for (BIter ti = make_iter(); ok && ti.valid(); ++ti.t, ti.settle()) {
+      for (auto ti = make_iter(); ok && ti.valid(); ++ti.t, ti.settle()) {
         const int32_t qy = static_cast<int32_t>(static_cast<int64_t>(bh) * p.S +
                                                 static_cast<int64_t>(ti.blk) * p.L +
                                                 static_cast<int64_t>(ti.t) * 128);
@@ -493,7 +494,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       mma_commit_e(bb.b(kBH + h));
     };
     bool issued = false, ok = true;
-    BIter ti = make_iter();
+    auto ti = make_iter();
     if (ti.valid() && mbar_wait(bb.b(kBA), 0, wd, abort_flag)) {
       tc_fence_after();
       int it = 0;  // Q_j in slot it, dO_j in it + 1
@@ -554,13 +555,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_bits + kColS + 64 * h, tP = tmem + lane_bits + kColP + 64 * h;
     const bool kvalid = row < nk;
-    const int64_t gk = p.causal ? zz_pos(b, min64(k0 + row, p.L - 1), C2, p.P) : 0;
+    const int64_t gk = CAUSAL ? zz_pos(b, min64(k0 + row, p.L - 1), C2, p.P) : 0;
     const float sl2 = p.scale_log2;
     // -LSE (log2 units) and -D of this half's 64 queries are staged in SMEM,
     // double-buffered: thread t < 64 holds query t's, thread 64 + t its -D,
     // read from global memory one tile ahead.
     const int qi = row & 63;
-    auto staged = [&](const BIter &t) -> float {
+    auto staged = [&](const BIter<CAUSAL> &t) -> float {
       const int64_t tq0 = static_cast<int64_t>(t.t) * 128;
       if (64 * h + qi >= min64(128, p.L - tq0)) return 0.f;
       const int64_t qrow = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(t.blk) * p.L +
@@ -568,10 +569,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       return row < 64 ? -(p.lse[qrow] * kLog2eB) : -p.Dv[qrow];
     };
     int j = 0;
-    BIter ti = make_iter();
+    auto ti = make_iter();
     float val = ti.valid() ? staged(ti) : 0.f;
     for (; ti.valid(); ++j) {
-      BIter tn = ti;
+      BIter<CAUSAL> tn = ti;
       ++tn.t;
       tn.settle();
       float *ld = sm_ld + (2 * h + (j & 1)) * 128;
@@ -589,7 +590,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       // Visible queries of this key: positions >= its own (a suffix of the tile).
       int first = 0, last = static_cast<int>(nq);
       if (!kvalid) first = last;
-      else if (p.causal) first = causal_visible(ti.blk, q0, gk - 1, p.L, p.P);
+      else if (CAUSAL) first = causal_visible(ti.blk, q0, gk - 1, p.L, p.P);
       if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBH + h), j & 1, wd, abort_flag))) break;
       tc_fence_after();
       // When every key row of the warp sees every query of this half, no
@@ -697,7 +698,7 @@ cudaError_t row_map_b(CUtensorMap *map, const void *base, int64_t rows, int d) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D>
+template <int D, bool CAUSAL>
 cudaError_t launch_bwd_variant(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                                const CUtensorMap &mdo, const BwdParams &p, int64_t units,
                                cudaStream_t stream) {
@@ -708,19 +709,20 @@ cudaError_t launch_bwd_variant(const CUtensorMap &mq, const CUtensorMap &mk, con
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  C::kSmemBytes)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D, CAUSAL>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes)) !=
+        cudaSuccess)
       return e;
-    if ((e = cudaFuncSetAttribute(bwd_dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  C::kSmemBytes)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(bwd_dkv_kernel<D, CAUSAL>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes)) !=
+        cudaSuccess)
       return e;
     configured[dev] = true;
   }
-  bwd_dq_kernel<D><<<static_cast<unsigned>(units), kThreadsB, C::kSmemBytes, stream>>>(mq, mk, mv,
-                                                                                       mdo, p);
+  const unsigned grid = static_cast<unsigned>(units);
+  bwd_dq_kernel<D, CAUSAL><<<grid, kThreadsB, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_dkv_kernel<D><<<static_cast<unsigned>(units), kThreadsB, C::kSmemBytes, stream>>>(mq, mk, mv,
-                                                                                        mdo, p);
+  bwd_dkv_kernel<D, CAUSAL><<<grid, kThreadsB, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
   return cudaGetLastError();
 }
 
@@ -743,8 +745,13 @@ cudaError_t launch_attn_bwd(const void *q, const void *k, const void *v, const v
   if ((e = row_map_b(&mk, k, rows, d)) != cudaSuccess) return e;
   if ((e = row_map_b(&mv, v, rows, d)) != cudaSuccess) return e;
   if ((e = row_map_b(&mdo, dout, rows, d)) != cudaSuccess) return e;
-  return d == 128 ? launch_bwd_variant<128>(mq, mk, mv, mdo, p, units, stream)
-                  : launch_bwd_variant<64>(mq, mk, mv, mdo, p, units, stream);
+  // The causal mask and tile skipping are compiled only into the causal
+  // instantiations.
+  if (d == 128)
+    return p.causal ? launch_bwd_variant<128, true>(mq, mk, mv, mdo, p, units, stream)
+                    : launch_bwd_variant<128, false>(mq, mk, mv, mdo, p, units, stream);
+  return p.causal ? launch_bwd_variant<64, true>(mq, mk, mv, mdo, p, units, stream)
+                  : launch_bwd_variant<64, false>(mq, mk, mv, mdo, p, units, stream);
 }
 
 }  // namespace ra
