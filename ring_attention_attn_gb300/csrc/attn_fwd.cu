@@ -38,6 +38,13 @@
 // The O rescale is lazy: a row's reference max only moves when the new max
 // exceeds it by more than 2^8 (in exp2 units), so P entries stay <= 256 and
 // the O accumulator in TMEM is touched only on such rare jumps.
+//
+// Compile-time variants (ring_attn_kernel<D, OUT_F32, PK, CAUSAL>): the head
+// dimension; fp32 per-step partials or normalised bf16 output; the tile
+// layout PK (0 row tiles, 1 packed short problems, 2 packed with 16 or 32
+// rows per problem so each softmax warp owns one 32-column chunk); and the
+// causal mask.  Code a variant does not use is not compiled into it, which
+// keeps the softmax warpgroups' registers for the work that is there.
 #include <math.h>
 
 #include "ra_device.cuh"
