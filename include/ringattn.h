@@ -209,7 +209,11 @@ int lse_merge(const float *o_parts, const float *lse_parts, int n, int64_t rows,
  *            each token over the N tokens of its own frame.
  *  temporal: out_t bf16 [B, H, T*N, d], lse_t fp32 [B, H, T*N]: attention of
  *            each token over the T tokens at its spatial position, run as a
- *            ring over P chunks of T/P frames (T % P == 0).
+ *            ring over P chunks of T/P frames (T % P == 0).  With every
+ *            chunk resident on one GPU, adjacent chunks of at most 32 frames
+ *            together may share a tile (12-frame chunks at P = 4 are taken
+ *            in pairs): the ring then has fewer, longer steps, and the
+ *            result differs only in the rounding order of the exact merge.
  * The two outputs are independent (not chained).  workspace: device memory
  * of at least factored_attn_workspace(...) bytes, 256-byte aligned, owned
  * by the caller and used as scratch by this call only. */

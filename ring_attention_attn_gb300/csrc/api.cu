@@ -665,10 +665,23 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
   }
   {
     ra::AttnParams p{};
-    const int64_t L = T / P;
+    // On one GPU every rank's chunk is resident, so packed tiles may fold f
+    // adjacent ranks' chunks (f divides P) into one block of f * T / P
+    // frames: the ring then runs over P / f such blocks.  Its merge over
+    // steps is exact, so folding changes only the rounding order, and the
+    // block-diagonal tile work shrinks by f (each query row of a tile meets
+    // one position's keys).  Folding stops at 32 rows per block (the
+    // warp-packed tiles) and keeps at least two blocks (a CTA's two query
+    // tiles): 12-frame chunks at P = 4 fold in pairs.
+    int f = 1;
+    if (packed)
+      for (int c = 2; c <= P / 2; ++c)
+        if (P % c == 0 && static_cast<int64_t>(c) * (T / P) <= 32) f = c;
+    const int Pr = P / f;  // ring size after folding
+    const int64_t L = T / Pr;
     p.BH = static_cast<int>(BH);
     p.G = N;
-    p.n_ranks = P;
+    p.n_ranks = Pr;
     p.n_stepgroups = 1;
     p.n_pairs = static_cast<int>((L + 255) / 256);
     p.q_rows_bh = S;
@@ -692,13 +705,13 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
       p.G = (N + pack - 1) / pack;
       p.L = static_cast<int64_t>(pack) * lrow;
       // Two ranks' chunks per CTA (its two query tiles share the key tiles).
-      p.n_ranks = (P + 1) / 2;
-      p.pack_ranks = P;
+      p.n_ranks = (Pr + 1) / 2;
+      p.pack_ranks = Pr;
       p.n_pairs = 1;
       p.pack_frame_major = 1;
     }
-    p.P = P;
-    p.steps_per_group = P;
+    p.P = Pr;
+    p.steps_per_group = Pr;
     p.scale_log2 = scale_log2(d);
     p.out = oT;
     p.lse = lT;

@@ -352,7 +352,10 @@ def test_allgather_reducescatter_forms_match_oracle(form, B, H, S, d, P, causal)
 
 
 # ---------------------------------------------------------------- factored --
-@pytest.mark.parametrize("B,H,T,N,d,P", [(1, 2, 8, 50, 64, 4),    # 2 rank pairs
+@pytest.mark.parametrize("B,H,T,N,d,P", [(1, 2, 8, 50, 64, 4),    # 2-frame chunks fold in pairs
+                                          (1, 2, 68, 20, 64, 4),   # 17-frame chunks: 2 rank pairs
+                                          (1, 1, 24, 30, 128, 6),  # 4-frame chunks fold by 3
+                                          (1, 2, 80, 7, 64, 5),    # P = 5: no fold, last unpaired
                                           (1, 2, 12, 50, 64, 3),   # odd P: last rank unpaired
                                           (2, 1, 6, 70, 128, 1),   # one rank
                                           (1, 3, 24, 40, 128, 2),
