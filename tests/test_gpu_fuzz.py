@@ -1,6 +1,7 @@
 """Seeded random shapes through the ring and factored entry points against the
 oracle: ragged chunk lengths, odd head counts, both head sizes, causal and
-not, P from 1 to 8, frame counts around the 16/32/128-row packing limits."""
+not, P from 1 to 8, frame counts around the 16/32/128-row packing limits and
+the folding of short rank chunks."""
 import numpy as np
 import pytest
 import torch
@@ -65,8 +66,9 @@ def test_ring_random_shapes(B, H, S, d, P, causal, seed):
 def _factored_cases():
     rng = np.random.default_rng(4242)
     cases = []
+    # (8, 8), (36, 6), (48, 8), (60, 4): short chunks that fold by 4, 3, 4, 2.
     for T, P in [(4, 4), (15, 5), (16, 1), (17, 1), (32, 2), (33, 3), (64, 2), (96, 3), (128, 1),
-                 (130, 2)]:
+                 (130, 2), (8, 8), (36, 6), (48, 8), (60, 4)]:
         N = int(rng.integers(3, 60))
         cases.append((1, int(rng.integers(1, 3)), T, N, int(rng.choice([64, 128])), P,
                       int(rng.integers(0, 1 << 30))))
