@@ -10,17 +10,19 @@
 // step s, as in the forward; block b's dK/dV gather the query chunks of the
 // ranks the block passes through, r = (b + s) mod P at step s.
 //
-// Three kernels:
+// Two launches:
 //   bwd_prep_kernel   D_i = dO_i . O_i (fp32), one warp per row.
-//   bwd_dq_kernel     one 128-row query tile per CTA.  Per K/V tile, in two
-//                     halves of 64 keys: S_h = Q K_h^T and dP_h = dO V_h^T
-//                     (SMEM operands) into TMEM; compute warpgroup h writes
-//                     dS_h (bf16) over S_h; dQ += dS_h K_h takes it from TMEM.
-//   bwd_dkv_kernel    one 128-key tile per CTA.  Per query tile, in two
-//                     halves of 64 queries: S^T_h = K Q_h^T and
-//                     dP^T_h = V dO_h^T; compute warpgroup h writes P^T_h
-//                     over S^T_h and dS^T_h over dP^T_h (bf16);
-//                     dV += P^T_h dO_h and dK += dS^T_h Q_h take them from TMEM.
+//   bwd_kernel        one CTA per unit of either kind (dK/dV units first, so
+//                     the shorter dQ units fill the launch's last wave):
+//     dQ unit         one 128-row query tile.  Per K/V tile, in two halves
+//                     of 64 keys: S_h = Q K_h^T and dP_h = dO V_h^T (SMEM
+//                     operands) into TMEM; compute warpgroup h writes dS_h
+//                     (bf16) over S_h; dQ += dS_h K_h takes it from TMEM.
+//     dK/dV unit      one 128-key tile.  Per query tile, in two halves of 64
+//                     queries: S^T_h = K Q_h^T and dP^T_h = V dO_h^T; compute
+//                     warpgroup h writes P^T_h over S^T_h and dS^T_h over
+//                     dP^T_h (bf16); dV += P^T_h dO_h and dK += dS^T_h Q_h
+//                     take them from TMEM.
 // Roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocation and
 // elected MMA issue, warps 4..7 / 8..11 compute warpgroups 0 / 1, one thread
 // per row of the tile and half h of its columns.  The halves pipeline: while
@@ -158,10 +160,9 @@ constexpr uint64_t kHalfRows = (64 * 128) >> 4;
 
 // ------------------------------------------------------------------ dQ ----
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreadsB, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const BwdParams p) {
+__device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                            const CUtensorMap &tm_v, const CUtensorMap &tm_do,
+                                            const BwdParams &p, int unit) {
   using C = BCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const Watchdog wd{p.wd.status, p.wd.limit_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  int u = blockIdx.x;
+  int u = unit;
   const int qt = u % p.n_t;
   u /= p.n_t;
   const int r = u % p.P;
@@ -390,10 +391,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
 // ---------------------------------------------------------------- dK/dV ----
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreadsB, 1)
-    bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                   const BwdParams p) {
+__device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                             const CUtensorMap &tm_v, const CUtensorMap &tm_do,
+                                             const BwdParams &p, int unit) {
   using C = BCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const Watchdog wd{p.wd.status, p.wd.limit_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  int u = blockIdx.x;
+  int u = unit;
   const int kt = u % p.n_t;
   u /= p.n_t;
   const int b = u % p.P;
@@ -667,6 +667,20 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 }
 
 // ---------------------------------------------------------------- host ----
+// One launch for both gradients: the first n_dkv CTAs run dK/dV units (the
+// longer ones), the rest dQ units, so the dQ units fill the dK/dV tail.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreadsB, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const BwdParams p, int n_dkv) {
+  const int b = static_cast<int>(blockIdx.x);
+  if (b < n_dkv)
+    bwd_dkv_body<D, CAUSAL>(tm_q, tm_k, tm_v, tm_do, p, b);
+  else
+    bwd_dq_body<D, CAUSAL>(tm_q, tm_k, tm_v, tm_do, p, b - n_dkv);
+}
+
 typedef CUresult (*EncodeTiledFnB)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -709,20 +723,15 @@ cudaError_t launch_bwd_variant(const CUtensorMap &mq, const CUtensorMap &mk, con
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D, CAUSAL>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes)) !=
-        cudaSuccess)
-      return e;
-    if ((e = cudaFuncSetAttribute(bwd_dkv_kernel<D, CAUSAL>,
+    if ((e = cudaFuncSetAttribute(bwd_kernel<D, CAUSAL>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes)) !=
         cudaSuccess)
       return e;
     configured[dev] = true;
   }
-  const unsigned grid = static_cast<unsigned>(units);
-  bwd_dq_kernel<D, CAUSAL><<<grid, kThreadsB, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_dkv_kernel<D, CAUSAL><<<grid, kThreadsB, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  const unsigned grid = static_cast<unsigned>(2 * units);
+  bwd_kernel<D, CAUSAL><<<grid, kThreadsB, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p,
+                                                                    static_cast<int>(units));
   return cudaGetLastError();
 }
 
@@ -733,7 +742,7 @@ cudaError_t launch_attn_bwd(const void *q, const void *k, const void *v, const v
   const int64_t rows = static_cast<int64_t>(p.BH) * p.S;
   if (rows == 0) return cudaSuccess;
   const int64_t units = static_cast<int64_t>(p.BH) * p.P * p.n_t;
-  if (units > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  if (2 * units > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const int64_t prep_blocks = (rows + 7) / 8;
   bwd_prep_kernel<<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16 *>(out), static_cast<const __nv_bfloat16 *>(dout), p.Dv, rows,
