@@ -50,6 +50,20 @@ float scale_log2(int d) { return static_cast<float>(1.4426950408889634 / sqrt(st
 
 int check_d(int d) { return (d == 64 || d == 128) ? RA_OK : RA_ERR_SHAPE; }
 
+// Rows per rank of the packed remainder tile for a launch of P ranks'
+// chunks of L rows (0: none).  A non-causal chunk ending in a short single
+// tile (L mod 256 in (0, 128], a multiple of 8 so the 128-byte swizzle
+// phase holds) has every rank's last rows stacked in one query tile when
+// they fit: one short unit per head instead of P, and the launch's last
+// wave no longer waits for them.
+int rem_pack_rows(int64_t L, int P, int causal) {
+  const int64_t n_pairs = (L + 255) / 256;
+  const int64_t rem = L - (n_pairs - 1) * 256;
+  if (causal || n_pairs < 2 || P < 2 || rem <= 0 || rem > 128 || rem % 8 != 0 || P * rem > 128)
+    return 0;
+  return static_cast<int>(rem);
+}
+
 // Largest row count a 2-D tensor map coordinate can address with a tile of
 // slack past the end.
 constexpr int64_t kMaxRows = (int64_t(1) << 31) - 512;
@@ -154,6 +168,7 @@ int ring_attn_fwd(const void *q, const void *k, const void *v, void *out, float 
   p.step_begin = 0;
   p.steps_per_group = P;
   p.causal = causal;
+  p.rem_pack = rem_pack_rows(L, P, causal);
   p.scale_log2 = scale_log2(d);
   p.out = out;
   p.lse = lse;
@@ -467,6 +482,7 @@ int cp_allgather_attn_fwd(const void *q, const void *k, const void *v, void *out
     p.rank_begin = 0;
     p.steps_per_group = P;
     p.causal = causal;
+    p.rem_pack = rem_pack_rows(L, P, causal);
     p.scale_log2 = scale_log2(d);
     p.out = out;
     p.lse = lse;

@@ -39,12 +39,14 @@
 // exceeds it by more than 2^8 (in exp2 units), so P entries stay <= 256 and
 // the O accumulator in TMEM is touched only on such rare jumps.
 //
-// Compile-time variants (ring_attn_kernel<D, OUT_F32, PK, CAUSAL>): the head
-// dimension; fp32 per-step partials or normalised bf16 output; the tile
+// Compile-time variants (ring_attn_kernel<D, OUT_F32, PK, CAUSAL, REM>): the
+// head dimension; fp32 per-step partials or normalised bf16 output; the tile
 // layout PK (0 row tiles, 1 packed short problems, 2 packed with 16 or 32
-// rows per problem so each softmax warp owns one 32-column chunk); and the
-// causal mask.  Code a variant does not use is not compiled into it, which
-// keeps the softmax warpgroups' registers for the work that is there.
+// rows per problem so each softmax warp owns one 32-column chunk); the
+// causal mask; and REM, launches whose ranks' short last tiles are stacked
+// into one query tile (rem_pack).  Code a variant does not use is not
+// compiled into it, which keeps the softmax warpgroups' registers for the
+// work that is there.
 #include <math.h>
 
 #include "ra_device.cuh"
@@ -97,14 +99,17 @@ __device__ __forceinline__ uint32_t col_o(int i) { return 256u + static_cast<uin
 struct Unit {
   int bh, g, rank, s_lo, s_hi, pair, part;
   int64_t q_row0;  // first row of the rank's query chunk in the Q tensor
+  bool rem;        // every rank's last rows in one tile (rem_pack)
 };
 
 // When a rank's last query-tile pair holds a single tile (L mod 256 <= 128),
 // its units cost about half of the others; they are numbered last so that
 // the block scheduler, which hands out CTAs in index order, packs them into
 // the final, partial wave (longest units first).
+template <bool REM>
 __device__ __forceinline__ Unit decode_unit(const AttnParams &p, int u) {
   Unit w;
+  w.rem = false;
   int np = p.n_pairs, pair_base = 0;
   if (p.n_pairs > 1 && p.L - static_cast<int64_t>(p.n_pairs - 1) * 2 * kBM <= kBM) {
     const int heavy = (p.n_pairs - 1) * p.n_stepgroups * p.n_ranks * p.G * p.BH;
@@ -114,6 +119,21 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams &p, int u) {
       u -= heavy;
       np = 1;
       pair_base = p.n_pairs - 1;
+      if (REM && p.rem_pack > 0) {
+        // One unit per (head, problem, step group) for all ranks' last rows.
+        w.rem = true;
+        w.pair = pair_base;
+        w.part = u % p.n_stepgroups;
+        u /= p.n_stepgroups;
+        w.g = u % p.G;
+        w.bh = u / p.G;
+        w.rank = p.rank_begin;
+        w.s_lo = p.step_begin + w.part * p.steps_per_group;
+        w.s_hi = w.s_lo + p.steps_per_group;
+        w.q_row0 =
+            static_cast<int64_t>(w.bh) * p.q_rows_bh + static_cast<int64_t>(w.g) * p.q_rows_g;
+        return w;
+      }
     }
   }
   w.pair = pair_base + u % np;
@@ -174,10 +194,10 @@ struct UnitGeo {
   bool has_q1;
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool REM>
 __device__ __forceinline__ UnitGeo unit_geo(const AttnParams &p, int u) {
   UnitGeo g;
-  g.w = decode_unit(p, u);
+  g.w = decode_unit<REM>(p, u);
   g.pair_row0 = static_cast<int64_t>(g.w.pair) * 2 * kBM;
   // Packed mode pairs rank chunks: tile 1 is the next rank's chunk.
   g.has_q1 = p.pack ? (p.pack_ranks > 0 && g.w.rank + 1 < p.rank_begin + p.pack_ranks)
@@ -187,15 +207,20 @@ __device__ __forceinline__ UnitGeo unit_geo(const AttnParams &p, int u) {
   return g;
 }
 
-template <int D, bool OUT_F32, int PK, bool CAUSAL>
+template <int D, bool OUT_F32, int PK, bool CAUSAL, bool REM>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p, int n_units) {
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_qr, const AttnParams p, int n_units) {
   using C = Cfg<D>;
   // PK: 0 = row tiles, 1 = packed short problems, 2 = packed with 16 or 32
   // rows per problem (warp-packed softmax).
   constexpr bool kPack = PK != 0;
+  // REM: launches with packed remainders (rem_pack > 0), bf16 non-causal
+  // row tiles only.
+  static_assert(!REM || (PK == 0 && !CAUSAL && !OUT_F32), "packed remainders: bf16 row tiles");
+  constexpr bool kRem = REM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -274,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int n_loaded = 0;  // Q pairs loaded
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const UnitGeo g = unit_geo<CAUSAL>(p, u);
+        const UnitGeo g = unit_geo<CAUSAL, kRem>(p, u);
         const Unit &w = g.w;
         TileIter ti;
         ti.init(p, w);
@@ -297,6 +322,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (g.has_q1)
               tma_load_4d(sbase + C::kOffQ1 + c * C::kChunkBytes, &tm_q, c * 64,
                           (w.rank + 1) * p.Lf, pn, w.bh, qfull);
+          }
+        } else if (kRem && w.rem) {
+          // rem_pack rows of each rank, stacked in the first query tile
+          // (rem_pack % 8 == 0 keeps the 128-byte swizzle phase).
+          const int rr = p.rem_pack;
+          const int64_t rstride = p.q_rank_stride ? p.q_rank_stride : p.L;
+          mbar_arrive_expect_tx(qfull, static_cast<uint32_t>(p.n_ranks * rr * 128 * C::kChunks));
+          for (int r = 0; r < p.n_ranks; ++r) {
+            const int32_t qy = static_cast<int32_t>(w.q_row0 + r * rstride + g.pair_row0);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_2d(sbase + C::kOffQ0 + c * C::kChunkBytes + r * rr * 128, &tm_qr, c * 64, qy,
+                          qfull);
           }
         } else {
           const int32_t qy = static_cast<int32_t>(w.q_row0 + g.pair_row0);
@@ -371,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int jt[2] = {0, 0};  // tiles handed to each softmax warpgroup so far
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const UnitGeo g = unit_geo<CAUSAL>(p, u);
+        const UnitGeo g = unit_geo<CAUSAL, kRem>(p, u);
         const Unit &w = g.w;
         const bool has_q1 = g.has_q1;
         const int nq = has_q1 ? 2 : 1;
@@ -463,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int jt = 0;      // tiles of this warpgroup so far (S_full / P_full phases)
     int n_done = 0;  // units whose O this warpgroup has read (O_done phases)
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const UnitGeo g = unit_geo<CAUSAL>(p, u);
+      const UnitGeo g = unit_geo<CAUSAL, kRem>(p, u);
       const Unit &w = g.w;
       if (!(wg == 0 || g.has_q1)) continue;
       // Row within the rank's chunk; in packed mode within the tile, whose
@@ -474,9 +512,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // hold the next frames and are not written) and sees only the first Lf
       // keys of that problem (columns [lo, lo + Lf) of a tile).
       const int pr = kPack ? static_cast<int>(qi / p.pLrow) : 0;
-      const bool row_valid =
+      bool row_valid =
           qi < p.L && (!kPack || (static_cast<int64_t>(w.g) * p.pack + pr < p.pN &&
                                    qi - static_cast<int64_t>(pr) * p.pLrow < p.Lf));
+      // Packed remainders: tile row r * rem_pack + i is row i of rank r's
+      // last rows (offset from the first rank's chunk).
+      int64_t rem_off = qi;
+      if (kRem && w.rem) {
+        const int rr = p.rem_pack;
+        row_valid = row < p.n_ranks * rr;
+        rem_off = static_cast<int64_t>(row / rr) * (p.q_rank_stride ? p.q_rank_stride : p.L) +
+                  g.pair_row0 + row % rr;
+      }
       const int64_t gq = CAUSAL ? zz_pos(w.rank, min64(qi, p.L - 1), p.L >> 1, p.P) : 0;
 
       float m_ref = -INFINITY, l = 0.f;
@@ -654,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t pf = static_cast<int64_t>(w.rank + wg) * p.Lf + (qi - static_cast<int64_t>(pr) * p.pLrow);
       const int64_t pn = static_cast<int64_t>(w.g) * p.pack + pr;
       const int64_t orow =
-          !kPack                 ? w.q_row0 + qi
+          !kPack                 ? w.q_row0 + rem_off
           : p.pack_frame_major ? (static_cast<int64_t>(w.bh) * p.pT + pf) * p.pN + pn
                                : (static_cast<int64_t>(w.bh) * p.pN + pn) * p.pT + pf;
       if (OUT_F32) {
@@ -774,12 +821,13 @@ EncodeTiledFn encode_fn() {
 
 // 2-D bf16 row matrix [rows, d], box = 128 rows x 64 elements (128 bytes),
 // 128-byte swizzle; rows past the end read as zero.
-cudaError_t make_row_map(CUtensorMap *map, const void *base, int64_t rows, int d) {
+cudaError_t make_row_map(CUtensorMap *map, const void *base, int64_t rows, int d,
+                         int box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -810,21 +858,33 @@ cudaError_t make_pack_map(CUtensorMap *map, const void *base, int64_t BH, int T,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, bool OUT_F32, int PK, bool CAUSAL>
-cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                           const AttnParams &p, int64_t n_units, cudaStream_t stream) {
+template <int D, bool OUT_F32, int PK, bool CAUSAL, bool REM>
+cudaError_t launch_kernel(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                          const CUtensorMap &mqr, const AttnParams &p, int64_t n_units,
+                          int64_t grid, int dev, cudaStream_t stream) {
   using C = Cfg<D>;
   static bool configured[64] = {};
+  if (!configured[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(ring_attn_kernel<D, OUT_F32, PK, CAUSAL, REM>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  ring_attn_kernel<D, OUT_F32, PK, CAUSAL, REM>
+      <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
+          mq, mk, mv, mqr, p, static_cast<int>(n_units));
+  return cudaGetLastError();
+}
+
+template <int D, bool OUT_F32, int PK, bool CAUSAL>
+cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                           const CUtensorMap &mqr, const AttnParams &p, int64_t n_units,
+                           cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(ring_attn_kernel<D, OUT_F32, PK, CAUSAL>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
   // Short units (a few key tiles each: 900-token frames, packed temporal
   // problems) run persistently, one CTA per SM walking units blockIdx.x,
   // + gridDim.x, ..., so that a CTA's next query pair and key tiles load
@@ -838,10 +898,13 @@ cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const C
   const int64_t tiles_per_unit = ((p.L + kBN - 1) / kBN) * p.steps_per_group;
   const int64_t grid =
       (tiles_per_unit <= kPersistMaxTiles && n_units > sms[dev]) ? sms[dev] : n_units;
-  ring_attn_kernel<D, OUT_F32, PK, CAUSAL>
-      <<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p,
-                                                                          static_cast<int>(n_units));
-  return cudaGetLastError();
+  if constexpr (PK == 0 && !CAUSAL && !OUT_F32) {
+    if (p.rem_pack > 0)
+      return launch_kernel<D, OUT_F32, PK, CAUSAL, true>(mq, mk, mv, mqr, p, n_units, grid, dev,
+                                                         stream);
+  }
+  return launch_kernel<D, OUT_F32, PK, CAUSAL, false>(mq, mk, mv, mqr, p, n_units, grid, dev,
+                                                      stream);
 }
 
 }  // namespace
@@ -849,10 +912,13 @@ cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const C
 cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k, const void *v,
                              int64_t kv_total_rows, int d, bool out_f32, const AttnParams &p,
                              cudaStream_t stream) {
-  const int64_t n_units = static_cast<int64_t>(p.BH) * p.G * p.n_ranks * p.n_stepgroups * p.n_pairs;
+  const int64_t per_pair = static_cast<int64_t>(p.BH) * p.G * p.n_stepgroups;
+  // With rem_pack every rank's single last tile shares one unit.
+  const int64_t n_units = p.rem_pack > 0 ? per_pair * ((p.n_pairs - 1) * p.n_ranks + 1)
+                                         : per_pair * p.n_ranks * p.n_pairs;
   if (n_units <= 0) return cudaSuccess;
   if (n_units > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mqr;
   cudaError_t e;
   if (p.pack) {
     if (out_f32 || p.causal || p.pLrow < p.Lf || p.pack * p.pLrow > kBM)
@@ -860,33 +926,41 @@ cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k,
     if ((e = make_pack_map(&mq, q, p.BH, p.pT, p.pN, p.pLrow, p.pack, d)) != cudaSuccess) return e;
     if ((e = make_pack_map(&mk, k, p.BH, p.pT, p.pN, p.pLrow, p.pack, d)) != cudaSuccess) return e;
     if ((e = make_pack_map(&mv, v, p.BH, p.pT, p.pN, p.pLrow, p.pack, d)) != cudaSuccess) return e;
+    mqr = mq;
     // Problems of 16 or 32 rows: every warp's rows and keys share one
     // 32-column chunk (the warp-packed softmax).
     const bool wp = p.pLrow == 16 || p.pLrow == 32;
     if (d == 128)
-      return wp ? launch_variant<128, false, 2, false>(mq, mk, mv, p, n_units, stream)
-                : launch_variant<128, false, 1, false>(mq, mk, mv, p, n_units, stream);
-    return wp ? launch_variant<64, false, 2, false>(mq, mk, mv, p, n_units, stream)
-              : launch_variant<64, false, 1, false>(mq, mk, mv, p, n_units, stream);
+      return wp ? launch_variant<128, false, 2, false>(mq, mk, mv, mqr, p, n_units, stream)
+                : launch_variant<128, false, 1, false>(mq, mk, mv, mqr, p, n_units, stream);
+    return wp ? launch_variant<64, false, 2, false>(mq, mk, mv, mqr, p, n_units, stream)
+              : launch_variant<64, false, 1, false>(mq, mk, mv, mqr, p, n_units, stream);
   } else {
     if ((e = make_row_map(&mq, q, q_total_rows, d)) != cudaSuccess) return e;
     if ((e = make_row_map(&mk, k, kv_total_rows, d)) != cudaSuccess) return e;
     if ((e = make_row_map(&mv, v, kv_total_rows, d)) != cudaSuccess) return e;
   }
+  if (p.rem_pack > 0) {
+    if (p.pack || p.causal || out_f32 || p.rem_pack % 8 != 0 || p.n_ranks * p.rem_pack > kBM)
+      return cudaErrorInvalidValue;
+    if ((e = make_row_map(&mqr, q, q_total_rows, d, p.rem_pack)) != cudaSuccess) return e;
+  } else {
+    mqr = mq;
+  }
   // Row tiles: the causal mask and the tile skipping it allows are compiled
   // only into the causal instantiations.
   if (d == 128) {
     if (p.causal)
-      return out_f32 ? launch_variant<128, true, 0, true>(mq, mk, mv, p, n_units, stream)
-                     : launch_variant<128, false, 0, true>(mq, mk, mv, p, n_units, stream);
-    return out_f32 ? launch_variant<128, true, 0, false>(mq, mk, mv, p, n_units, stream)
-                   : launch_variant<128, false, 0, false>(mq, mk, mv, p, n_units, stream);
+      return out_f32 ? launch_variant<128, true, 0, true>(mq, mk, mv, mqr, p, n_units, stream)
+                     : launch_variant<128, false, 0, true>(mq, mk, mv, mqr, p, n_units, stream);
+    return out_f32 ? launch_variant<128, true, 0, false>(mq, mk, mv, mqr, p, n_units, stream)
+                   : launch_variant<128, false, 0, false>(mq, mk, mv, mqr, p, n_units, stream);
   }
   if (p.causal)
-    return out_f32 ? launch_variant<64, true, 0, true>(mq, mk, mv, p, n_units, stream)
-                   : launch_variant<64, false, 0, true>(mq, mk, mv, p, n_units, stream);
-  return out_f32 ? launch_variant<64, true, 0, false>(mq, mk, mv, p, n_units, stream)
-                 : launch_variant<64, false, 0, false>(mq, mk, mv, p, n_units, stream);
+    return out_f32 ? launch_variant<64, true, 0, true>(mq, mk, mv, mqr, p, n_units, stream)
+                   : launch_variant<64, false, 0, true>(mq, mk, mv, mqr, p, n_units, stream);
+  return out_f32 ? launch_variant<64, true, 0, false>(mq, mk, mv, mqr, p, n_units, stream)
+                 : launch_variant<64, false, 0, false>(mq, mk, mv, mqr, p, n_units, stream);
 }
 
 cudaError_t launch_watchdog_selftest(const WatchdogParams &wd, cudaStream_t stream) {

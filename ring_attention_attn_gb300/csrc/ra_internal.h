@@ -57,6 +57,12 @@ struct AttnParams {
   // Per-step partials indexed by the K/V block that produced them
   // ((rank - step) mod P) instead of by step (reduce-scatter form).
   int part_by_block;
+  // Row tiles, non-causal, every rank's chunk ending in a short single tile:
+  // when rem_pack > 0 one unit per (head, problem, step group) holds the
+  // last rem_pack rows of each of the n_ranks chunks in one query tile
+  // (rank r at tile rows [r * rem_pack, (r + 1) * rem_pack)), meeting the
+  // key tiles in the first rank's ring order.
+  int rem_pack;
   WatchdogParams wd;
 };
 

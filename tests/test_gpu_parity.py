@@ -124,6 +124,11 @@ CASES = [
     (2, 2, 520, 64, 2, True),
     (1, 1, 16, 64, 8, True),
     (1, 3, 2048, 128, 8, False),
+    # chunks ending in a short tile whose rows all ranks stack in one tile
+    (1, 2, 1088, 64, 4, False),   # 272-row chunks: 4 x 16 rows
+    (1, 3, 888, 128, 3, False),   # 296-row chunks: 3 x 40 rows
+    (2, 1, 2112, 64, 8, False),   # 264-row chunks: 8 x 8 rows
+    (1, 1, 656, 128, 2, False),   # 328-row chunks: 2 x 72 rows do not fit
 ]
 
 
