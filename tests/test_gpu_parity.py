@@ -342,7 +342,8 @@ def _per_rank(x, P, layout):
 
 @pytest.mark.parametrize("form", ["allgather", "reducescatter"])
 @pytest.mark.parametrize("B,H,S,d,P,causal", [(1, 2, 1024, 128, 4, False), (1, 2, 2048, 64, 2, True),
-                                              (2, 1, 600, 128, 3, True), (1, 3, 1000, 64, 8, False)])
+                                              (2, 1, 600, 128, 3, True), (1, 3, 1000, 64, 8, False),
+                                              (1, 2, 1088, 128, 4, False)])  # stacked last rows
 def test_allgather_reducescatter_forms_match_oracle(form, B, H, S, d, P, causal):
     layout = 1 if causal else 0
     q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=S + 5 * P + causal)
