@@ -23,6 +23,9 @@
 //                     warpgroup h writes P^T_h over S^T_h and dS^T_h over
 //                     dP^T_h (bf16); dV += P^T_h dO_h and dK += dS^T_h Q_h
 //                     take them from TMEM.
+//   Non-causal chunks whose last tile is short stack every chunk's last rows
+//   (queries for dQ, keys for dK/dV) into one tile per head (REM variants):
+//   one unit instead of P nearly empty ones.
 // Roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocation and
 // elected MMA issue, warps 4..7 / 8..11 compute warpgroups 0 / 1, one thread
 // per row of the tile and half h of its columns.  The halves pipeline: while
@@ -159,9 +162,10 @@ __device__ __forceinline__ void issue_acc_k64(uint32_t d_tmem, uint32_t a_tmem, 
 constexpr uint64_t kHalfRows = (64 * 128) >> 4;
 
 // ------------------------------------------------------------------ dQ ----
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool REM>
 __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                             const CUtensorMap &tm_v, const CUtensorMap &tm_do,
+                                            const CUtensorMap &tm_qr, const CUtensorMap &tm_dor,
                                             const BwdParams &p, int unit) {
   using C = BCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -174,14 +178,24 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUten
   const Watchdog wd{p.wd.status, p.wd.limit_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // With REM, units past BH * P * (n_t - 1) stack every rank's last rows.
   int u = unit;
-  const int qt = u % p.n_t;
-  u /= p.n_t;
-  const int r = u % p.P;
-  const int bh = u / p.P;
+  const int nt_full = REM ? p.n_t - 1 : p.n_t;
+  const bool stacked = REM && u >= p.BH * p.P * nt_full;
+  int qt, r, bh;
+  if (stacked) {
+    qt = p.n_t - 1;
+    r = 0;
+    bh = u - p.BH * p.P * nt_full;
+  } else {
+    qt = u % nt_full;
+    u /= nt_full;
+    r = u % p.P;
+    bh = u / p.P;
+  }
   const int64_t C2 = p.L >> 1;
   const int64_t q0 = static_cast<int64_t>(qt) * 128;
-  const int64_t nq = min64(128, p.L - q0);
+  const int64_t nq = stacked ? static_cast<int64_t>(p.P) * p.rem : min64(128, p.L - q0);
   const int64_t q_row0 = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(r) * p.L + q0;
   const int64_t gq_max = CAUSAL ? zz_pos(r, q0 + nq - 1, C2, p.P) : 0;
   auto make_iter = [&]() {
@@ -213,13 +227,29 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUten
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(bb.b(kBA), 2 * C::kTile);
+      if (stacked) {
+        // Each rank's rem last rows of Q and dO, stacked (rem % 8 == 0 keeps
+        // the 128-byte swizzle phase).
+        mbar_arrive_expect_tx(bb.b(kBA), static_cast<uint32_t>(2 * p.P * p.rem * 128 * C::kChunks));
+        for (int rr = 0; rr < p.P; ++rr) {
+          const int32_t y = static_cast<int32_t>(q_row0 + static_cast<int64_t>(rr) * p.L);
 #pragma unroll
-      for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes, &tm_q, c * 64,
-                    static_cast<int32_t>(q_row0), bb.b(kBA));
-        tma_load_2d(sbase + C::kOffB + c * C::kChunkBytes, &tm_do, c * 64,
-                    static_cast<int32_t>(q_row0), bb.b(kBA));
+          for (int c = 0; c < C::kChunks; ++c) {
+            tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes + rr * p.rem * 128, &tm_qr, c * 64, y,
+                        bb.b(kBA));
+            tma_load_2d(sbase + C::kOffB + c * C::kChunkBytes + rr * p.rem * 128, &tm_dor, c * 64,
+                        y, bb.b(kBA));
+          }
+        }
+      } else {
+        mbar_arrive_expect_tx(bb.b(kBA), 2 * C::kTile);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes, &tm_q, c * 64,
+                      static_cast<int32_t>(q_row0), bb.b(kBA));
+          tma_load_2d(sbase + C::kOffB + c * C::kChunkBytes, &tm_do, c * 64,
+                      static_cast<int32_t>(q_row0), bb.b(kBA));
+        }
       }
       int it = 0;
       bool ok = true;
@@ -317,7 +347,8 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUten
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_bits + kColS + 64 * h, tP = tmem + lane_bits + kColP + 64 * h;
     const bool valid = row < nq;
-    const int64_t grow = q_row0 + row;
+    const int64_t grow =
+        stacked ? q_row0 + static_cast<int64_t>(row / p.rem) * p.L + row % p.rem : q_row0 + row;
     const float lse2 = valid ? p.lse[grow] * kLog2eB : 0.f;
     const float Drow = valid ? p.Dv[grow] : 0.f;
     const int64_t gq = CAUSAL ? zz_pos(r, min64(q0 + row, p.L - 1), C2, p.P) : 0;
@@ -390,9 +421,10 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUten
 }
 
 // ---------------------------------------------------------------- dK/dV ----
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool REM>
 __device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                              const CUtensorMap &tm_v, const CUtensorMap &tm_do,
+                                             const CUtensorMap &tm_kr, const CUtensorMap &tm_vr,
                                              const BwdParams &p, int unit) {
   using C = BCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -406,14 +438,24 @@ __device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUte
   const Watchdog wd{p.wd.status, p.wd.limit_ns};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // With REM, units past BH * P * (n_t - 1) stack every block's last keys.
   int u = unit;
-  const int kt = u % p.n_t;
-  u /= p.n_t;
-  const int b = u % p.P;
-  const int bh = u / p.P;
+  const int nt_full = REM ? p.n_t - 1 : p.n_t;
+  const bool stacked = REM && u >= p.BH * p.P * nt_full;
+  int kt, b, bh;
+  if (stacked) {
+    kt = p.n_t - 1;
+    b = 0;
+    bh = u - p.BH * p.P * nt_full;
+  } else {
+    kt = u % nt_full;
+    u /= nt_full;
+    b = u % p.P;
+    bh = u / p.P;
+  }
   const int64_t C2 = p.L >> 1;
   const int64_t k0 = static_cast<int64_t>(kt) * 128;
-  const int64_t nk = min64(128, p.L - k0);
+  const int64_t nk = stacked ? static_cast<int64_t>(p.P) * p.rem : min64(128, p.L - k0);
   const int64_t k_row0 = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(b) * p.L + k0;
   const int64_t gk_min = CAUSAL ? zz_pos(b, k0, C2, p.P) : 0;
   auto make_iter = [&]() {
@@ -447,13 +489,27 @@ __device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUte
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(bb.b(kBA), 2 * C::kTile);
+      if (stacked) {
+        mbar_arrive_expect_tx(bb.b(kBA), static_cast<uint32_t>(2 * p.P * p.rem * 128 * C::kChunks));
+        for (int rr = 0; rr < p.P; ++rr) {
+          const int32_t y = static_cast<int32_t>(k_row0 + static_cast<int64_t>(rr) * p.L);
 #pragma unroll
-      for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes, &tm_k, c * 64,
-                    static_cast<int32_t>(k_row0), bb.b(kBA));
-        tma_load_2d(sbase + C::kOffB + c * C::kChunkBytes, &tm_v, c * 64,
-                    static_cast<int32_t>(k_row0), bb.b(kBA));
+          for (int c = 0; c < C::kChunks; ++c) {
+            tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes + rr * p.rem * 128, &tm_kr, c * 64, y,
+                        bb.b(kBA));
+            tma_load_2d(sbase + C::kOffB + c * C::kChunkBytes + rr * p.rem * 128, &tm_vr, c * 64, y,
+                        bb.b(kBA));
+          }
+        }
+      } else {
+        mbar_arrive_expect_tx(bb.b(kBA), 2 * C::kTile);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes, &tm_k, c * 64,
+                      static_cast<int32_t>(k_row0), bb.b(kBA));
+          tma_load_2d(sbase + C::kOffB + c * C::kChunkBytes, &tm_v, c * 64,
+                      static_cast<int32_t>(k_row0), bb.b(kBA));
+        }
       }
       int it = 0;
       bool ok = true;
@@ -639,7 +695,8 @@ __device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUte
       const bool have = j > 0 && __all_sync(0xffffffffu, mbar_wait(bb.b(kBO), 0, wd, abort_flag));
       tc_fence_after();
       // Warpgroup 0 writes the dV row, warpgroup 1 the dK row.
-      const int64_t grow = k_row0 + row;
+      const int64_t grow =
+          stacked ? k_row0 + static_cast<int64_t>(row / p.rem) * p.L + row % p.rem : k_row0 + row;
       const uint32_t tA = tmem + lane_bits + (h == 0 ? kColAcc0 : kColAcc1);
       __nv_bfloat16 *dst = (h == 0 ? p.dv : p.dk) + grow * D;
       const float mul = h == 0 ? 1.f : p.scale;
@@ -669,16 +726,19 @@ __device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUte
 // ---------------------------------------------------------------- host ----
 // One launch for both gradients: the first n_dkv CTAs run dK/dV units (the
 // longer ones), the rest dQ units, so the dQ units fill the dK/dV tail.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool REM>
 __global__ void __launch_bounds__(kThreadsB, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_kr,
+               const __grid_constant__ CUtensorMap tm_vr, const __grid_constant__ CUtensorMap tm_dor,
                const BwdParams p, int n_dkv) {
+  static_assert(!(REM && CAUSAL), "stacked last tiles: non-causal only");
   const int b = static_cast<int>(blockIdx.x);
   if (b < n_dkv)
-    bwd_dkv_body<D, CAUSAL>(tm_q, tm_k, tm_v, tm_do, p, b);
+    bwd_dkv_body<D, CAUSAL, REM>(tm_q, tm_k, tm_v, tm_do, tm_kr, tm_vr, p, b);
   else
-    bwd_dq_body<D, CAUSAL>(tm_q, tm_k, tm_v, tm_do, p, b - n_dkv);
+    bwd_dq_body<D, CAUSAL, REM>(tm_q, tm_k, tm_v, tm_do, tm_qr, tm_dor, p, b - n_dkv);
 }
 
 typedef CUresult (*EncodeTiledFnB)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -699,12 +759,13 @@ EncodeTiledFnB encode_fn_b() {
   return fn;
 }
 
-cudaError_t row_map_b(CUtensorMap *map, const void *base, int64_t rows, int d) {
+cudaError_t row_map_b(CUtensorMap *map, const void *base, int64_t rows, int d,
+                      int box_rows = 128) {
   EncodeTiledFnB fn = encode_fn_b();
   if (!fn) return cudaErrorNotSupported;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -712,9 +773,8 @@ cudaError_t row_map_b(CUtensorMap *map, const void *base, int64_t rows, int d) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, bool CAUSAL>
-cudaError_t launch_bwd_variant(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                               const CUtensorMap &mdo, const BwdParams &p, int64_t units,
+template <int D, bool CAUSAL, bool REM>
+cudaError_t launch_bwd_variant(const CUtensorMap *maps, const BwdParams &p, int64_t units,
                                cudaStream_t stream) {
   using C = BCfg<D>;
   static bool configured[64] = {};
@@ -723,25 +783,35 @@ cudaError_t launch_bwd_variant(const CUtensorMap &mq, const CUtensorMap &mk, con
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    if ((e = cudaFuncSetAttribute(bwd_kernel<D, CAUSAL>,
+    if ((e = cudaFuncSetAttribute(bwd_kernel<D, CAUSAL, REM>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes)) !=
         cudaSuccess)
       return e;
     configured[dev] = true;
   }
   const unsigned grid = static_cast<unsigned>(2 * units);
-  bwd_kernel<D, CAUSAL><<<grid, kThreadsB, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p,
-                                                                    static_cast<int>(units));
+  bwd_kernel<D, CAUSAL, REM><<<grid, kThreadsB, C::kSmemBytes, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], p,
+      static_cast<int>(units));
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attn_bwd(const void *q, const void *k, const void *v, const void *out,
-                            const void *dout, int d, const BwdParams &p, cudaStream_t stream) {
+                            const void *dout, int d, const BwdParams &params,
+                            cudaStream_t stream) {
+  BwdParams p = params;
   const int64_t rows = static_cast<int64_t>(p.BH) * p.S;
   if (rows == 0) return cudaSuccess;
-  const int64_t units = static_cast<int64_t>(p.BH) * p.P * p.n_t;
+  // Non-causal chunks ending in a short tile: every chunk's last rows share
+  // one tile per head (and kind of unit) when they fit.
+  const int64_t rem = p.L - static_cast<int64_t>(p.n_t - 1) * 128;
+  p.rem = (!p.causal && p.n_t > 1 && p.P > 1 && rem < 128 && rem % 8 == 0 && p.P * rem <= 128)
+              ? static_cast<int>(rem)
+              : 0;
+  const int64_t units = p.rem ? static_cast<int64_t>(p.BH) * (p.P * (p.n_t - 1) + 1)
+                              : static_cast<int64_t>(p.BH) * p.P * p.n_t;
   if (2 * units > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const int64_t prep_blocks = (rows + 7) / 8;
   bwd_prep_kernel<<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
@@ -749,18 +819,28 @@ cudaError_t launch_attn_bwd(const void *q, const void *k, const void *v, const v
       d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  CUtensorMap mq, mk, mv, mdo;
-  if ((e = row_map_b(&mq, q, rows, d)) != cudaSuccess) return e;
-  if ((e = row_map_b(&mk, k, rows, d)) != cudaSuccess) return e;
-  if ((e = row_map_b(&mv, v, rows, d)) != cudaSuccess) return e;
-  if ((e = row_map_b(&mdo, dout, rows, d)) != cudaSuccess) return e;
+  // q, k, v, dO with 128-row boxes, then with rem-row boxes (stacked tiles).
+  CUtensorMap maps[8];
+  const void *src[4] = {q, k, v, dout};
+  for (int i = 0; i < 4; ++i) {
+    if ((e = row_map_b(&maps[i], src[i], rows, d)) != cudaSuccess) return e;
+    if (p.rem) {
+      if ((e = row_map_b(&maps[4 + i], src[i], rows, d, p.rem)) != cudaSuccess) return e;
+    } else {
+      maps[4 + i] = maps[i];
+    }
+  }
+  // Kernel parameter order: q, k, v, dO, then the stacked maps q, k, v, dO.
   // The causal mask and tile skipping are compiled only into the causal
-  // instantiations.
-  if (d == 128)
-    return p.causal ? launch_bwd_variant<128, true>(mq, mk, mv, mdo, p, units, stream)
-                    : launch_bwd_variant<128, false>(mq, mk, mv, mdo, p, units, stream);
-  return p.causal ? launch_bwd_variant<64, true>(mq, mk, mv, mdo, p, units, stream)
-                  : launch_bwd_variant<64, false>(mq, mk, mv, mdo, p, units, stream);
+  // instantiations, the stacked last tiles only into the REM ones.
+  if (d == 128) {
+    if (p.causal) return launch_bwd_variant<128, true, false>(maps, p, units, stream);
+    return p.rem ? launch_bwd_variant<128, false, true>(maps, p, units, stream)
+                 : launch_bwd_variant<128, false, false>(maps, p, units, stream);
+  }
+  if (p.causal) return launch_bwd_variant<64, true, false>(maps, p, units, stream);
+  return p.rem ? launch_bwd_variant<64, false, true>(maps, p, units, stream)
+               : launch_bwd_variant<64, false, false>(maps, p, units, stream);
 }
 
 }  // namespace ra

@@ -75,6 +75,11 @@ struct BwdParams {
   const float *lse;  // forward LSE [BH, S]
   float *Dv;         // D_i = dO_i . O_i [BH, S] (scratch, written by the prep kernel)
   __nv_bfloat16 *dq, *dk, *dv;
+  // Non-causal chunks whose last tile holds rem < 128 rows (rem % 8 == 0,
+  // P * rem <= 128): one unit per head of each kind stacks every chunk's
+  // last rows in one tile (chunk r at tile rows [r * rem, (r + 1) * rem)).
+  // Set by launch_attn_bwd; 0 = off.
+  int rem;
   WatchdogParams wd;
 };
 

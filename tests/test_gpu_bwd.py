@@ -33,6 +33,8 @@ CASES = [
     (1, 1, 256, 128, 1, True),
     (1, 3, 1000, 128, 4, False),
     (1, 1, 16, 64, 8, True),
+    (1, 2, 1088, 128, 4, False),  # 272-row chunks: the ranks' last 16 rows stacked
+    (1, 1, 504, 64, 3, False),    # 168-row chunks: 3 x 40 rows stacked
 ]
 
 
