@@ -322,6 +322,9 @@ int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out
     p.step_begin = s;
     p.steps_per_group = 1;
     p.causal = causal;
+    // Stacked last rows read rank 0's current block for every rank: over the
+    // P steps each rank's rows still meet every block once.
+    p.rem_pack = rem_pack_rows(L, P, causal);
     p.scale_log2 = scale_log2(d);
     p.out = o_parts + static_cast<size_t>(s) * BH * S * d;
     p.lse = l_parts + static_cast<size_t>(s) * BH * S;
@@ -529,6 +532,9 @@ int cp_reducescatter_attn_fwd(const void *q, const void *k, const void *v, void 
     p.steps_per_group = 1;
     p.causal = causal;
     p.part_by_block = 1;
+    // Stacked last rows meet rank 0's block of each step and file the
+    // partial under that block.
+    p.rem_pack = rem_pack_rows(L, P, causal);
     p.scale_log2 = scale_log2(d);
     p.out = o_parts;
     p.lse = l_parts;

@@ -217,9 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // PK: 0 = row tiles, 1 = packed short problems, 2 = packed with 16 or 32
   // rows per problem (warp-packed softmax).
   constexpr bool kPack = PK != 0;
-  // REM: launches with packed remainders (rem_pack > 0), bf16 non-causal
-  // row tiles only.
-  static_assert(!REM || (PK == 0 && !CAUSAL && !OUT_F32), "packed remainders: bf16 row tiles");
+  // REM: launches with packed remainders (rem_pack > 0), non-causal row
+  // tiles only.
+  static_assert(!REM || (PK == 0 && !CAUSAL), "packed remainders: non-causal row tiles");
   constexpr bool kRem = REM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -898,7 +898,7 @@ cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const C
   const int64_t tiles_per_unit = ((p.L + kBN - 1) / kBN) * p.steps_per_group;
   const int64_t grid =
       (tiles_per_unit <= kPersistMaxTiles && n_units > sms[dev]) ? sms[dev] : n_units;
-  if constexpr (PK == 0 && !CAUSAL && !OUT_F32) {
+  if constexpr (PK == 0 && !CAUSAL) {
     if (p.rem_pack > 0)
       return launch_kernel<D, OUT_F32, PK, CAUSAL, true>(mq, mk, mv, mqr, p, n_units, grid, dev,
                                                          stream);
@@ -941,7 +941,7 @@ cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k,
     if ((e = make_row_map(&mv, v, kv_total_rows, d)) != cudaSuccess) return e;
   }
   if (p.rem_pack > 0) {
-    if (p.pack || p.causal || out_f32 || p.rem_pack % 8 != 0 || p.n_ranks * p.rem_pack > kBM)
+    if (p.pack || p.causal || p.rem_pack % 8 != 0 || p.n_ranks * p.rem_pack > kBM)
       return cudaErrorInvalidValue;
     if ((e = make_row_map(&mqr, q, q_total_rows, d, p.rem_pack)) != cudaSuccess) return e;
   } else {

@@ -285,7 +285,8 @@ def test_c5_full_size_sampled():
 # ------------------------------------------------- overlapped ring copies --
 @pytest.mark.parametrize("B,H,S,d,P,causal,separate",
                          [(1, 2, 2048, 128, 4, False, True), (1, 2, 4096, 64, 2, True, True),
-                          (2, 1, 1200, 128, 3, True, False), (1, 3, 1000, 64, 8, False, True)])
+                          (2, 1, 1200, 128, 3, True, False), (1, 3, 1000, 64, 8, False, True),
+                          (1, 2, 1088, 128, 4, False, True)])  # stacked last rows
 def test_overlap_ring_matches_oracle_and_fused(B, H, S, d, P, causal, separate):
     layout = 1 if causal else 0
     q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=S + 11 * P + causal)
