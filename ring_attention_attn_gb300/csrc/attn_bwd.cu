@@ -14,10 +14,12 @@
 //   bwd_prep_kernel   D_i = dO_i . O_i (fp32), one warp per row.
 //   bwd_kernel        one CTA per unit of either kind (dK/dV units first, so
 //                     the shorter dQ units fill the launch's last wave):
-//     dQ unit         one 128-row query tile.  Per K/V tile, in two halves
-//                     of 64 keys: S_h = Q K_h^T and dP_h = dO V_h^T (SMEM
-//                     operands) into TMEM; compute warpgroup h writes dS_h
-//                     (bf16) over S_h; dQ += dS_h K_h takes it from TMEM.
+//     dQ unit         one 128-row query tile, whose Q and dO the compute
+//                     warpgroups first copy into TMEM.  Per K/V tile, in two
+//                     halves of 64 keys: S_h = Q K_h^T and dP_h = dO V_h^T
+//                     (Q, dO from TMEM, K, V from SMEM) into TMEM; compute
+//                     warpgroup h writes dS_h (bf16) over S_h; dQ += dS_h K_h
+//                     takes it from TMEM.
 //     dK/dV unit      one 128-key tile.  Per query tile, in two halves of 64
 //                     queries: S^T_h = K Q_h^T and dP^T_h = V dO_h^T; compute
 //                     warpgroup h writes P^T_h over S^T_h and dS^T_h over
@@ -71,6 +73,31 @@ enum : int { kBA = 0, kBH = 1, kBC = 3, kBO = 5, kBDrain = 6, kBLd = 7, kBKV = k
 constexpr int kBTmemSlot = 496;
 constexpr int kBAbort = 500;
 constexpr uint32_t kColS = 0, kColP = 128, kColAcc0 = 256, kColAcc1 = 384;
+// dQ units: Q at kColQT and dO at kColQT + D/2 (bf16 pairs), the A operands
+// of S and dP straight from tensor memory; kBQT (256 arrivals) = both copied.
+constexpr uint32_t kColQT = 384;
+constexpr int kBQT = 7;
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// D[tmem] = A[tmem] B[smem]^T over d: A (128 rows x d, bf16 pairs, 8 columns
+// per 16 elements) from tensor memory, B K-major with the 128-byte swizzle.
+template <int D>
+__device__ __forceinline__ void issue_qk_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t db,
+                                            uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+    mma_ts_e(d_tmem, a_tmem + kk * 8, db + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
 
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ out,
                                                        const __nv_bfloat16 *__restrict__ dout,
@@ -212,6 +239,7 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUten
     }
     mbar_init(bb.b(kBO), 1);
     mbar_init(bb.b(kBDrain), 1);
+    mbar_init(bb.b(kBQT), 256);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(bb.kv_full0 + 8 * s, 1);
       mbar_init(bb.kv_empty0 + 8 * s, 1);
@@ -276,22 +304,21 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUten
     constexpr uint32_t idesc_h = idesc_bf16_f32(128, 64, 0, 0);
     constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
     constexpr uint32_t kSlotDesc = C::kTile >> 4;
-    const uint64_t dQd = smem_desc_sw128(sbase + C::kOffA, 16, 1024);
-    const uint64_t dOd = smem_desc_sw128(sbase + C::kOffB, 16, 1024);
     const uint64_t dKV = smem_desc_sw128(sbase + C::kOffKV, 16, 1024);
     const uint64_t dKVmn = smem_desc_sw128(sbase + C::kOffKV, C::kChunkBytes, 1024);
     // S_h = Q K_h^T and dP_h = dO V_h^T for the 64 keys of half h of the
     // K/V tiles in slots ks, vs.
     auto issue_s = [&](int h, int ks, int vs) {
-      issue_qk<D>(tmem + kColS + 64 * h, dQd,
-                  dKV + static_cast<uint64_t>(ks * kSlotDesc) + h * kHalfRows, idesc_h);
-      issue_qk<D>(tmem + kColP + 64 * h, dOd,
-                  dKV + static_cast<uint64_t>(vs * kSlotDesc) + h * kHalfRows, idesc_h);
+      issue_qk_ts<D>(tmem + kColS + 64 * h, tmem + kColQT,
+                     dKV + static_cast<uint64_t>(ks * kSlotDesc) + h * kHalfRows, idesc_h);
+      issue_qk_ts<D>(tmem + kColP + 64 * h, tmem + kColQT + D / 2,
+                     dKV + static_cast<uint64_t>(vs * kSlotDesc) + h * kHalfRows, idesc_h);
       mma_commit_e(bb.b(kBH + h));
     };
     bool issued = false, ok = true;
     auto ti = make_iter();
-    if (ti.valid() && mbar_wait(bb.b(kBA), 0, wd, abort_flag)) {
+    // Q and dO reach tensor memory through the compute warpgroups.
+    if (ti.valid() && mbar_wait(bb.b(kBQT), 0, wd, abort_flag)) {
       tc_fence_after();
       int it = 0;  // K_j in slot it, V_j in it + 1
       ok = mbar_wait(bb.kv_full0 + 8 * (it % C::kSlots), (it / C::kSlots) & 1, wd, abort_flag) &&
@@ -355,6 +382,29 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUten
     const float sl2 = p.scale_log2;
     const float2 sl2v = make_float2(sl2, sl2), nlse2 = make_float2(-lse2, -lse2),
                  nD2 = make_float2(-Drow, -Drow);
+    // Warpgroup 0 copies this row of Q, warpgroup 1 of dO, from the swizzled
+    // shared-memory tile (16-byte piece c of a 128-byte row segment sits at
+    // piece c ^ (row % 8)) into tensor memory as bf16 pairs.
+    if (__all_sync(0xffffffffu, mbar_wait(bb.b(kBA), 0, wd, abort_flag))) {
+      const uint32_t src = sbase + (h == 0 ? C::kOffA : C::kOffB) + row * 128;
+      const uint32_t dst = tmem + lane_bits + kColQT + (D / 2) * h;
+#pragma unroll
+      for (int k = 0; k < D / 64; ++k) {
+        uint32_t u0[16], u1[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 a = ld_shared_v4(src + k * C::kChunkBytes + ((c ^ (row & 7)) << 4));
+          const uint4 b = ld_shared_v4(src + k * C::kChunkBytes + (((c + 4) ^ (row & 7)) << 4));
+          u0[4 * c] = a.x; u0[4 * c + 1] = a.y; u0[4 * c + 2] = a.z; u0[4 * c + 3] = a.w;
+          u1[4 * c] = b.x; u1[4 * c + 1] = b.y; u1[4 * c + 2] = b.z; u1[4 * c + 3] = b.w;
+        }
+        tmem_st16(dst + k * 32, u0);
+        tmem_st16(dst + k * 32 + 16, u1);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bb.b(kBQT));
+    }
     int j = 0;
     for (auto ti = make_iter(); ti.valid(); ++j, ++ti.t, ti.settle()) {
       if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBH + h), j & 1, wd, abort_flag))) break;
