@@ -358,6 +358,33 @@ def test_allgather_reducescatter_forms_match_oracle(form, B, H, S, d, P, causal)
     _cmp(o, l, ro, rl)
 
 
+# ---------------------------------- every CP form at 14,400 tokens (sampled) --
+@pytest.mark.parametrize("form", ["overlap", "ulysses", "allgather", "reducescatter"])
+def test_cp_forms_c3_sampled_rows(form):
+    """The 14,400-token workload (3,600-row chunks: each rank's last 16 rows
+    stacked into one tile) through every context-parallel form, on the rows
+    the ring test samples."""
+    w = synth.WORKLOADS["c3"]
+    q, k, v = synth.make_qkv(w)
+    B, H, S, d, P = w.B, w.H, w.S, w.d, w.P
+    if form == "overlap":
+        o, l = ra.ring_attn_fwd_overlap(q.cuda(), k.cuda(), v.cuda(), P,
+                                        comm_stream=torch.cuda.Stream())
+        o, l = o.cpu(), l.cpu()
+    else:
+        fn = {"ulysses": ra.ulysses_attn_fwd, "allgather": ra.cp_allgather_attn_fwd,
+              "reducescatter": ra.cp_reducescatter_attn_fwd}[form]
+        o, l = fn(*(_seq_split(x, P).cuda() for x in (q, k, v)), B, H, S, P)
+        o = o.cpu().permute(1, 2, 0, 3, 4).reshape(B, H, S, d)
+        l = l.cpu().permute(1, 2, 0, 3).reshape(B, H, S)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+    per = synth.sample_rows(w, 48)
+    rows = oracle.flat_rows(B, H, S, per)
+    ro, rl = oracle.attention(q, k, v, rows=rows)
+    _cmp(o.reshape(-1, d)[rows], l.reshape(-1)[rows], ro, rl)
+
+
 # ---------------------------------------------------------------- factored --
 @pytest.mark.parametrize("B,H,T,N,d,P", [(1, 2, 8, 50, 64, 4),    # 2-frame chunks fold in pairs
                                           (1, 2, 68, 20, 64, 4),   # 17-frame chunks: 2 rank pairs
