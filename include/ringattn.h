@@ -83,7 +83,10 @@ int ra_frame_transpose(const void *x, void *y, int64_t BH, int64_t T, int64_t N,
  * (r - s) mod P for s = 0..P-1; scores are masked by global token position
  * (key <= query) when causal.  Requires S % P == 0 (S % 2P == 0 if causal).
  * Result equals full attention ("mathematically equivalent to full-sequence
- * attention", ultralytics glossary, "How Context Parallelism Works"). */
+ * attention", ultralytics glossary, "How Context Parallelism Works").  When
+ * non-causal chunks end in a short tile (S/P mod 256 in (0, 128], a multiple
+ * of 8, P times it at most 128), every rank's last rows are computed
+ * together in rank 0's block order; only the rounding order differs. */
 int ring_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B,
                   int H, int64_t S, int d, int P, int causal, void *stream);
 
@@ -134,7 +137,10 @@ size_t ring_attn_fwd_overlap_workspace(int B, int H, int64_t S, int d, int P);
  * lse (the forward LSE): fp32 [B, H, S], all in sharded order with the same
  * P and causal flag as the forward.  Rank r's dQ visits the K/V blocks in the
  * forward's ring order; block b's dK/dV gather the query chunks of ranks
- * b, b+1, ... (the order the block travels the ring).  workspace: at least
+ * b, b+1, ... (the order the block travels the ring).  Non-causal chunks
+ * whose last 128-row tile is short (a multiple of 8 rows, P times it at most
+ * 128) have those rows of every rank (or block) taken together, in rank 0's
+ * (block 0's) order; only the rounding order differs.  workspace: at least
  * ring_attn_bwd_workspace(...) bytes (fp32 D), 256-byte aligned, used by this
  * call only.  dq, dk, dv must not overlap the inputs. */
 int ring_attn_bwd(const void *q, const void *k, const void *v, const void *out, const float *lse,
