@@ -116,7 +116,9 @@ int ring_attn_fwd_rank(const void *q_local, const void *k, const void *v, void *
  * queries to the block in its current buffer (block (r - s) mod P) while
  * `comm_stream` copies each rank's current block into the next buffer of rank
  * r + 1 (2P device-to-device copies per step).  Each step writes fp32 partials
- * (workspace), merged at the end by the lse_merge kernel on `stream`.
+ * (workspace), merged at the end by the lse_merge kernel on `stream`.  Stacked
+ * last rows (as in ring_attn_fwd) read rank 0's current block at every step,
+ * so each rank's last rows still meet every block once.
  * comm_stream may equal stream (copies then serialise with compute).
  * workspace: >= ring_attn_fwd_overlap_workspace(...) bytes, 256-byte aligned,
  * used by this call only.  Events are created and released internally. */
@@ -189,6 +191,8 @@ size_t ulysses_attn_workspace(int B, int H, int64_t S, int d);
  *                             yields a partial (O, LSE) for every query; the
  *                             partials of each query are merged (the reduce)
  *                             and each rank's rows are scattered back.
+ * Both stack every rank's short last rows as ring_attn_fwd does (the
+ * reduce-scatter form files their partials under the block they read).
  * workspace: >= cp_variant_workspace(...) bytes (either form), 256-byte
  * aligned, used by this call only. */
 int cp_allgather_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
