@@ -1,7 +1,8 @@
 """Seeded random shapes through the ring and factored entry points against the
 oracle: ragged chunk lengths, odd head counts, both head sizes, causal and
 not, P from 1 to 8, frame counts around the 16/32/128-row packing limits and
-the folding of short rank chunks."""
+the folding of short rank chunks, and chunks whose short last rows every
+form (and the backward) stacks into one tile."""
 import numpy as np
 import pytest
 import torch
@@ -85,3 +86,52 @@ def test_factored_random_shapes(B, H, T, N, d, P, seed):
     _cmp(os_, ls, ro, rl)
     ro, rl = oracle.factored(q, k, v, T, N, "temporal")
     _cmp(ot, lt, ro, rl)
+
+
+def _stacked_cases():
+    """Non-causal chunks of npairs * 256 + rem rows (rem a multiple of 8,
+    P * rem <= 128): every rank's last rem rows share one query tile."""
+    rng = np.random.default_rng(7770)
+    cases = []
+    for i in range(6):
+        P = int(rng.choice([2, 3, 4, 5, 8]))
+        rem = int(rng.choice([8, 16, 24, 32, 40, 48, 64]))
+        if P * rem > 128:
+            rem = 8 * max(1, (128 // P) // 8)
+        L = int(rng.integers(1, 4)) * 256 + rem
+        cases.append((1, int(rng.integers(1, 3)), P * L, 64 if i % 2 else 128, P,
+                      int(rng.integers(0, 1 << 30))))
+    return cases
+
+
+@pytest.mark.parametrize("B,H,S,d,P,seed", _stacked_cases())
+def test_stacked_last_rows_every_form(B, H, S, d, P, seed):
+    q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=seed)
+    ro, rl = oracle.attention(q, k, v)
+    o, l = ra.ring_attn_fwd(q.cuda(), k.cuda(), v.cuda(), P)
+    _cmp(o, l, ro, rl)
+    o, l = ra.ring_attn_fwd_overlap(q.cuda(), k.cuda(), v.cuda(), P)
+    _cmp(o, l, ro, rl)
+    L = S // P
+    per_rank = [x.reshape(B, H, P, L, d).permute(2, 0, 1, 3, 4).contiguous().cuda()
+                for x in (q, k, v)]
+    for fn in (ra.cp_allgather_attn_fwd, ra.cp_reducescatter_attn_fwd):
+        o, l = fn(*per_rank, B, H, S, P)
+        _cmp(o.cpu().permute(1, 2, 0, 3, 4).reshape(B, H, S, d),
+             l.cpu().permute(1, 2, 0, 3).reshape(B, H, S), ro, rl)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+
+
+@pytest.mark.parametrize("B,H,S,d,P,seed", _stacked_cases()[:4])
+def test_stacked_last_rows_backward(B, H, S, d, P, seed):
+    """Gradients with every chunk's last rows stacked (queries for dQ, keys
+    for dK/dV); bound as in the backward parity tests."""
+    q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=seed)
+    g, _, _ = synth.make_custom((B, H, S, d), (1, 1, 1, 1), seed=seed + 1)
+    o, l = ra.ring_attn_fwd(q.cuda(), k.cuda(), v.cuda(), P)
+    grads = ra.ring_attn_bwd(q.cuda(), k.cuda(), v.cuda(), o, l, g.cuda(), P)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+    for a, r in zip(grads, oracle.attention_bwd(q, k, v, g)):
+        assert np.max(np.abs(a.double().cpu().numpy() - r)) <= 1e-2 * np.max(np.abs(r)) + 1e-3
