@@ -500,10 +500,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                          31u) == 0;
     int jt = 0;      // tiles of this warpgroup so far (S_full / P_full phases)
     int n_done = 0;  // units whose O this warpgroup has read (O_done phases)
+    // The next unit's geometry is decoded while the last PV of the current
+    // one runs, off the path from this unit's epilogue to the next S.
+    UnitGeo g_next = unit_geo<CAUSAL, kRem>(p, blockIdx.x);
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const UnitGeo g = unit_geo<CAUSAL, kRem>(p, u);
+      const UnitGeo g = g_next;
+      const int u_next = u + static_cast<int>(gridDim.x);
       const Unit &w = g.w;
-      if (!(wg == 0 || g.has_q1)) continue;
+      if (!(wg == 0 || g.has_q1)) {
+        if (u_next < n_units) g_next = unit_geo<CAUSAL, kRem>(p, u_next);
+        continue;
+      }
       // Row within the rank's chunk; in packed mode within the tile, whose
       // rank is w.rank + wg.
       const int64_t qi = kPack ? row : g.pair_row0 + wg * kBM + row;
@@ -684,6 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
       if (aborted) break;
+      if (u_next < n_units) g_next = unit_geo<CAUSAL, kRem>(p, u_next);
       bool have_o = false;
       if (j > 0) {
         have_o = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarODone + wg), n_done & 1, wd,
