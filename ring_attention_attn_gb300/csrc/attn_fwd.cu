@@ -503,6 +503,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The next unit's geometry is decoded while the last PV of the current
     // one runs, off the path from this unit's epilogue to the next S.
     UnitGeo g_next = unit_geo<CAUSAL, kRem>(p, blockIdx.x);
+    // Packed tiles: this thread's row is frame row_fr of problem row_pr in
+    // every unit.
+    const int row_pr = kPack ? row / p.pLrow : 0;
+    const int row_fr = kPack ? row - row_pr * p.pLrow : 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       const UnitGeo g = g_next;
       const int u_next = u + static_cast<int>(gridDim.x);
@@ -518,10 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // g * pack + qi / pLrow (pLrow >= Lf rows per problem; rows past Lf
       // hold the next frames and are not written) and sees only the first Lf
       // keys of that problem (columns [lo, lo + Lf) of a tile).
-      const int pr = kPack ? static_cast<int>(qi / p.pLrow) : 0;
+      const int pr = row_pr;
       bool row_valid =
           qi < p.L && (!kPack || (static_cast<int64_t>(w.g) * p.pack + pr < p.pN &&
-                                   qi - static_cast<int64_t>(pr) * p.pLrow < p.Lf));
+                                   row_fr < p.Lf));
       // Packed remainders: tile row r * rem_pack + i is row i of rank r's
       // last rows (offset from the first rank's chunk).
       int64_t rem_off = qi;
@@ -706,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int part = p.part_by_block ? ((w.rank - w.s_lo) % p.P + p.P) % p.P : w.part;
       // Packed mode: frame f = (w.rank + wg) * Lf + qi % pLrow of position
       // n = g * pack + qi / pLrow.
-      const int64_t pf = static_cast<int64_t>(w.rank + wg) * p.Lf + (qi - static_cast<int64_t>(pr) * p.pLrow);
+      const int64_t pf = static_cast<int64_t>(w.rank + wg) * p.Lf + row_fr;
       const int64_t pn = static_cast<int64_t>(w.g) * p.pack + pr;
       const int64_t orow =
           !kPack                 ? w.q_row0 + rem_off
