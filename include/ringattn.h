@@ -57,9 +57,10 @@ extern "C" {
  * caller (either may be NULL).  Errors: RA_ERR_ARG, RA_ERR_SHAPE. */
 int ra_cp_shard_index(int64_t S, int P, int layout, int64_t *s2g, int64_t *g2s);
 
-/* KV block that rank r holds at ring step s: (r - s) mod P (k8ai ring
- * diagram: at step 1 GPU0 gets K/V3, GPU1 gets K/V0).  Host only.  Returns -1
- * on bad arguments. */
+/* KV block that rank r holds at ring step s: (r - s) mod P (k8ai "Sequence
+ * and Context Parallel", ring diagram: after the first exchange rank 0 holds
+ * block 3 and rank 1 holds block 0 of four).  Host only.  Returns -1 on bad
+ * arguments. */
 int ra_ring_source(int P, int rank, int step);
 
 /* Row permutation of a bf16 [BH, S, d] tensor between global and sharded
@@ -82,8 +83,8 @@ int ra_frame_transpose(const void *x, void *y, int64_t BH, int64_t T, int64_t N,
  * [B, H, S], both in sharded order.  Rank r's queries visit KV blocks
  * (r - s) mod P for s = 0..P-1; scores are masked by global token position
  * (key <= query) when causal.  Requires S % P == 0 (S % 2P == 0 if causal).
- * Result equals full attention ("mathematically equivalent to full-sequence
- * attention", ultralytics glossary, "How Context Parallelism Works").  When
+ * The result is exact full attention over the whole sequence (ultralytics
+ * glossary, "How Context Parallelism Works").  When
  * non-causal chunks end in a short tile (S/P mod 256 in (0, 128], a multiple
  * of 8, P times it at most 128), every rank's last rows are computed
  * together in rank 0's block order; only the rounding order differs. */
@@ -107,10 +108,10 @@ int ring_attn_fwd_rank(const void *q_local, const void *k, const void *v, void *
                        int causal, int step_begin, int step_end, int out_fp32, void *stream);
 
 /* Ring attention with the K/V exchange performed as real copies, overlapped
- * with the attention of the current step ("Because the sends overlap with
- * compute on the current block, you can hide most of the communication
- * latency", "day 83" blog, "Context parallelism: splitting the sequence";
- * k8ai ring diagram: send next while computing current).  Same inputs,
+ * with the attention of the current step: while a rank works on the block it
+ * holds, the next block is already travelling, so the transfer time hides
+ * behind compute ("day 83" blog, "Context parallelism: splitting the
+ * sequence"; k8ai "Sequence and Context Parallel", ring diagram).  Same inputs,
  * outputs and result as ring_attn_fwd.  Every simulated rank r owns a K/V
  * double buffer in `workspace`; at step s the compute stream attends rank r's
  * queries to the block in its current buffer (block (r - s) mod P) while
@@ -129,8 +130,8 @@ int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out
 /* Workspace bytes of ring_attn_fwd_overlap (0 on bad arguments). */
 size_t ring_attn_fwd_overlap_workspace(int B, int H, int64_t S, int d, int P);
 
-/* Backward pass of ring_attn_fwd ("Ring exchanges happen in every attention
- * layer, forward and backward", k8ai "Sequence and Context Parallel",
+/* Backward pass of ring_attn_fwd (the ring's exchanges recur in the backward
+ * pass of every attention layer: k8ai "Sequence and Context Parallel",
  * "Communication profile").  Gradients of the loss with upstream gradient
  * dout = dL/dO:  P_ij = exp(q_i.k_j / sqrt(d) - LSE_i),  D_i = dO_i . O_i,
  *   dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (dO_i . v_j - D_i),
@@ -153,8 +154,8 @@ int ring_attn_bwd(const void *q, const void *k, const void *v, const void *out, 
 size_t ring_attn_bwd_workspace(int B, int H, int64_t S);
 
 /* Ulysses all-to-all (k8ai "Sequence and Context Parallel", "An alternative:
- * all-to-all on heads": switch from split-by-sequence to split-by-heads
- * around attention, then back).  Row permutation of a bf16 tensor of
+ * all-to-all on heads": the tokens are re-split by head for the attention
+ * and re-split by sequence afterwards).  Row permutation of a bf16 tensor of
  * B*H*S rows of d elements between two per-rank layouts (P divides H):
  *   sequence-split  [P][B][H][L][d]    rank r holds its L = S/P tokens of every head;
  *   head-split      [P][B][H/P][S][d]  rank r holds heads r*H/P .. of every token
@@ -177,10 +178,9 @@ int ulysses_attn_fwd(const void *q, const void *k, const void *v, void *out, flo
 /* Workspace bytes of ulysses_attn_fwd (0 on bad arguments). */
 size_t ulysses_attn_workspace(int B, int H, int64_t S, int d);
 
-/* The all-gather and reduce-scatter forms of context parallelism ("the NVIDIA
- * context parallel package describes all-gather, reduce-scatter, and
- * ring-based communication options", ultralytics glossary, "How Context
- * Parallelism Works").  q, k, v, out: bf16 per-rank buffers [P][B][H][L][d]
+/* The all-gather and reduce-scatter forms of context parallelism, the two
+ * communication patterns the glossary lists beside the ring (ultralytics
+ * glossary, "How Context Parallelism Works").  q, k, v, out: bf16 per-rank buffers [P][B][H][L][d]
  * (rank r's L = S/P tokens of every head, in the order ra_cp_shard gives its
  * chunk: contiguous, or zigzag when causal); lse: fp32 [P][B][H][L].  Both
  * equal full attention.
@@ -203,9 +203,8 @@ int cp_reducescatter_attn_fwd(const void *q, const void *k, const void *v, void 
                               size_t ws_bytes, void *stream);
 size_t cp_variant_workspace(int B, int H, int64_t S, int d, int P);
 
-/* Online-softmax merge of n normalised partials of the same rows ("the online
- * softmax trick", "day 83" blog, "Context parallelism: splitting the
- * sequence"):  M = max_i LSE_i,  w_i = exp(LSE_i - M),
+/* Online-softmax merge of n normalised partials of the same rows ("day 83"
+ * blog, "Context parallelism: splitting the sequence"):  M = max_i LSE_i,  w_i = exp(LSE_i - M),
  *   LSE = M + ln(sum w_i),  O = sum w_i O_i / sum w_i;
  * rows whose partials are all empty (LSE = -inf) get O = 0, LSE = -inf.
  * o_parts fp32 [n][rows][d], lse_parts fp32 [n][rows]; out bf16 [rows][d],
@@ -231,12 +230,13 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
                   void *out_t, float *lse_t, int B, int H, int T, int N, int d, int P,
                   void *workspace, size_t ws_bytes, void *stream);
 
-/* Scratch bytes factored_attn needs for these sizes (0 on bad arguments).
- * 0 when T <= 128: every rank chunk (T/P frames) then fits one 128-row tile
- * and the temporal pass reads and writes the frame-major tensors in place.
- * For T > 128, room for position-major copies of q, k, v and of the temporal
- * output (bf16) and LSE (fp32), used when a chunk is longer than 128 frames.
- * With a 0 result the workspace pointer may be null. */
+/* Scratch bytes that suffice for factored_attn at these sizes with any P
+ * (0 on bad arguments).  0 when T <= 128.  For T > 128: room for
+ * position-major copies of q, k, v and of the temporal output (bf16) and LSE
+ * (fp32).  A call only uses them when its rank chunks are longer than 128
+ * frames (T / P > 128); with chunks of up to 128 frames the temporal pass
+ * reads and writes the frame-major tensors in place, factored_attn checks no
+ * workspace and the pointer may be null, whatever this function returns. */
 size_t factored_attn_workspace(int B, int H, int T, int N, int d);
 
 /* Size of the fixed device scratch that factored_attn_static works in. */
@@ -250,15 +250,23 @@ size_t factored_attn_workspace(int B, int H, int T, int N, int d);
  * whose device memory is all handed to its own pool at start-up, or a serving
  * loop in which an allocation (and the synchronisation cudaMalloc implies) is
  * not allowed.
- *  - Limit: the sizes must satisfy factored_attn_workspace(B,H,T,N,d) <=
- *    RA_STATIC_SCRATCH_BYTES: any size with T <= 128 (no scratch needed),
- *    for T > 128 about 65,000 tokens x heads at d = 128 and 130,000 at
- *    d = 64; larger sizes return RA_ERR_WORKSPACE and launch nothing.  Other
- *    argument errors are those of factored_attn.
+ *  - Limit: any size whose rank chunks hold at most 128 frames (T / P <= 128)
+ *    needs no scratch and is accepted.  Longer chunks need
+ *    factored_attn_workspace(B,H,T,N,d) <= RA_STATIC_SCRATCH_BYTES: about
+ *    65,000 tokens x heads at d = 128 and 130,000 at d = 64; larger sizes
+ *    return RA_ERR_WORKSPACE and launch nothing.  Other argument errors are
+ *    those of factored_attn.
  *  - The array lives in every GPU that loads the library until the process
  *    exits.  The first call on a device looks up the array's device address
  *    (once per device, with that device current); make that first call before
- *    any stream capture.
+ *    any stream capture.  The CUDA runtime loads device code lazily by
+ *    default, so that first call is also when the 64 MiB array is placed in
+ *    the device's memory: it can fail there with RA_ERR_CUDA (out of memory)
+ *    if the caller's own pool has already taken all device memory.  Make the
+ *    first call (any sizes) before creating such a pool.
+ *  - The looked-up address is kept for the life of the process: after
+ *    cudaDeviceReset, or after the primary context is destroyed and made
+ *    again, this entry point must not be called on that device.
  *  - Nothing in the scratch needs to start at zero (every byte read is first
  *    written by the same call), but all calls share the one array: calls whose
  *    work overlaps on the GPU (other streams, other host threads) race; order

@@ -9,8 +9,8 @@ fp64 loops, OpenMP over query rows) and, for tiny shapes, in ``brute.py``
 
 Citations (page title, section):
   * full attention is the target of the ring method -- ultralytics glossary
-    "Context Parallelism", "How Context Parallelism Works" (mathematically
-    equivalent to full-sequence attention);
+    "Context Parallelism", "How Context Parallelism Works" (the ring's answer
+    is exact full attention);
   * ring schedule and online-softmax accumulation -- "day 83" blog, "Context
     parallelism: splitting the sequence"; k8ai "Sequence and Context
     Parallel", "How context parallel works" (ring diagram);
@@ -18,8 +18,8 @@ Citations (page title, section):
     zigzag (2P chunks, rank r holds chunks r and 2P-1-r);
   * factored spatial / temporal attention -- "day 83" blog, "The
     spatial-temporal twist";
-  * the backward pass ("Ring exchanges happen in every attention layer,
-    forward and backward", k8ai "Communication profile"; the glossary's
+  * the backward pass (the ring's exchanges recur in the backward pass of
+    every attention layer, k8ai "Communication profile"; the glossary's
     example calls .backward()) -- the gradients of the full-attention
     definition.
 """

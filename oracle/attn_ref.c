@@ -7,9 +7,9 @@
  *
  * What it computes (sources are the three pages on context parallelism):
  *
- *  - Full softmax attention, the definition the ring method must reproduce:
- *    "The final result is mathematically equivalent to full-sequence
- *    attention" (ultralytics glossary, "How Context Parallelism Works"); the
+ *  - Full softmax attention, the definition the ring method must reproduce
+ *    exactly: the ring's answer is full attention over the whole sequence
+ *    (ultralytics glossary, "How Context Parallelism Works"); the
  *    43,200 x 43,200 score matrix of the "day 83" blog intro.
  *      s_ij  = (q_i . k_j) / sqrt(d)
  *      LSE_i = ln sum_{j in K(i)} exp(s_ij)
@@ -19,8 +19,8 @@
  *
  *  - Ring attention as the pages describe it, step by step: every rank keeps
  *    its query chunk; at step s rank r holds KV block (r - s) mod P (k8ai
- *    "How context parallel works", ring diagram: at step 1 GPU0 gets K/V3,
- *    GPU1 gets K/V0); each block's partial result is folded into a running
+ *    "How context parallel works", ring diagram: after the first exchange
+ *    rank 0 holds block 3 and rank 1 holds block 0); each block's partial result is folded into a running
  *    (max, sum, output) with the online-softmax rule (day 83 blog, "Context
  *    parallelism: splitting the sequence").  Used only to pin ring == full.
  *
@@ -182,7 +182,8 @@ int oracle_factored(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 /* ------------------------------------------------------------ ring form -- */
 
 /* Block held by rank r at ring step s: at step 0 its own, then the block of
- * the rank before it (k8ai ring diagram: step 1, GPU0 gets K/V3, GPU1 K/V0). */
+ * the rank before it (k8ai ring diagram: after one exchange rank 0 holds block 3, rank 1
+ * block 0). */
 int64_t oracle_ring_source(int64_t P, int64_t r, int64_t s)
 {
     return ((r - s) % P + P) % P;

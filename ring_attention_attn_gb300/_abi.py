@@ -343,11 +343,13 @@ def factored_attn(q, k, v, T: int, N: int, P: int, workspace=None, outs=None, st
     """Spatial (within frame) and temporal (across frames, ring over P) attention.
 
     Returns (out_s, lse_s, out_t, lse_t).  workspace: uint8 CUDA tensor of at
-    least factored_attn_workspace(...) bytes (allocated here if None).
+    least factored_attn_workspace(...) bytes, needed only when the rank chunks
+    exceed 128 frames (T / P > 128; allocated here if None).
     """
     import torch
     B, H, S, d = q.shape
-    need = factored_attn_workspace(B, H, T, N, d)
+    chunks_fit = P > 0 and T % P == 0 and T // P <= 128
+    need = 0 if chunks_fit else factored_attn_workspace(B, H, T, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     if outs is None:

@@ -1,6 +1,6 @@
 // Ring-attention backward for sm_103a: gradients dQ, dK, dV of the forward
-// in attn_fwd.cu ("Ring exchanges happen in every attention layer, forward
-// and backward", k8ai "Sequence and Context Parallel", "Communication
+// in attn_fwd.cu (the ring's exchanges recur in the backward pass of every
+// attention layer: k8ai "Sequence and Context Parallel", "Communication
 // profile").  With s_ij = scale q_i.k_j, P_ij = exp(s_ij - LSE_i) (LSE from
 // the forward) and D_i = dO_i . O_i:
 //     dP_ij = dO_i . v_j,   dS_ij = P_ij (dP_ij - D_i),

@@ -1,7 +1,8 @@
 // Online-softmax merge of normalised partial attention outputs.
 //
-// "Each GPU accumulates partial attention outputs using the online softmax
-// trick" ("day 83" blog, "Context parallelism: splitting the sequence").  For
+// Every rank folds the partial results of the blocks it meets into one
+// answer with the online-softmax rule ("day 83" blog, "Context parallelism:
+// splitting the sequence"); this kernel is that fold over n partials.  For
 // n partials (O_i, LSE_i) of the same query row:
 //   M = max_i LSE_i,  w_i = exp(LSE_i - M),  LSE = M + ln sum_i w_i,
 //   O = sum_i w_i O_i / sum_i w_i;   all LSE_i = -inf  ->  O = 0, LSE = -inf.

@@ -20,7 +20,10 @@ static __device__ __align__(256) unsigned char g_factored_scratch[RA_STATIC_SCRA
 
 // Device address of the scratch on the current device, looked up once per
 // device (with that device current) and cached.  nullptr on failure, with the
-// CUDA error recorded.
+// CUDA error recorded.  The runtime loads the library's device code lazily,
+// so this first lookup is also where the array is placed in device memory.
+// The cache is never refreshed: after cudaDeviceReset (or the primary context
+// being torn down) the cached address is stale, which the header states.
 void *scratch_on_current_device() {
   static void *addr[64] = {};
   static std::mutex mu;
@@ -52,10 +55,11 @@ void *scratch_on_current_device() {
 extern "C" int factored_attn_static(const void *q, const void *k, const void *v, void *out_s,
                                     float *lse_s, void *out_t, float *lse_t, int B, int H, int T,
                                     int N, int d, int P, void *stream) {
-  // Sizes beyond the fixed scratch are refused before anything runs.
-  // (factored_attn_workspace returns 0 for invalid sizes; factored_attn then
-  // reports the argument error itself.)
-  const size_t need = factored_attn_workspace(B, H, T, N, d);
+  // Sizes beyond the fixed scratch are refused before anything runs.  The
+  // count is the one this P needs: chunks of up to 128 frames use no scratch
+  // whatever T is.  (Invalid sizes count 0 here; factored_attn then reports
+  // the argument error itself.)
+  const size_t need = ra::factored_scratch_bytes(B, H, T, N, d, P);
   if (need > RA_STATIC_SCRATCH_BYTES) return RA_ERR_WORKSPACE;
   void *ws = scratch_on_current_device();
   if (ws == nullptr) return RA_ERR_CUDA;

@@ -103,6 +103,11 @@ cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int n
 // Watchdog self-test kernel (attn_fwd.cu).
 cudaError_t launch_watchdog_selftest(const WatchdogParams &wd, cudaStream_t stream);
 
+// Scratch bytes factored_attn uses for these sizes and this P (api.cu): 0
+// when every rank chunk of T / P frames fits one tile, otherwise
+// factored_attn_workspace(B, H, T, N, d).
+size_t factored_scratch_bytes(int B, int H, int T, int N, int d, int P);
+
 // Records `e` as the error ra_last_cuda_error reports; returns RA_ERR_CUDA (api.cu).
 int record_cuda_error(cudaError_t e);
 

@@ -147,3 +147,25 @@ def sample_rows(w: Workload | str, per_head: int, index: int | None = None):
         if c not in chosen:
             chosen.append(c)
     return np.array(sorted(chosen[:per_head]), dtype=np.int64)
+
+
+def tile_rows(n_heads: int, n_rows: int, chunk: int, tile: int = 128, salt: int = 0):
+    """Flat row indices (head * n_rows + row) with one row in every `tile`-row
+    query tile of every `chunk`-row chunk of every head.
+
+    Tile t of chunk c in head h contributes row c*chunk + t*tile + lane, with
+    lane = (37*t + 53*h + 11*c + salt) mod (rows of that tile), so that over
+    the tiles every lane position of a full tile is met, and a short last tile
+    contributes a different one of its rows per chunk and head.
+    """
+    out = []
+    n_chunks = n_rows // chunk
+    n_t = (chunk + tile - 1) // tile
+    for h in range(n_heads):
+        for c in range(n_chunks):
+            t = np.arange(n_t, dtype=np.int64)
+            rows_in_tile = np.minimum(tile, chunk - t * tile)
+            lane = (37 * t + 53 * h + 11 * c + salt) % rows_in_tile
+            r = t * tile + lane
+            out.append(h * n_rows + c * chunk + r)
+    return np.unique(np.concatenate(out)) if out else np.empty(0, dtype=np.int64)

@@ -140,12 +140,20 @@ def test_ring_small_cases(B, H, S, d, P, causal):
     _cmp(o, l, ro, rl)
 
 
-def test_ring_c3_sampled_rows():
+def _c3_rows(w):
+    """One row in every 128-row query tile of every rank chunk and head of the
+    14,400-token workload (2,784 rows, the lane rotating from tile to tile),
+    plus the first and last row of each chunk."""
+    rows = synth.tile_rows(w.B * w.H, w.S, w.L)
+    edge = oracle.flat_rows(w.B, w.H, w.S, synth.sample_rows(w, 2 * w.P))
+    return np.unique(np.concatenate([rows, edge]))
+
+
+def test_ring_c3_every_tile():
     w = synth.WORKLOADS["c3"]
     q, k, v = synth.make_qkv(w)
     o, l = _run_ring(q, k, v, w.P, w.causal)
-    per = synth.sample_rows(w, 48)
-    rows = oracle.flat_rows(w.B, w.H, w.S, per)
+    rows = _c3_rows(w)
     ro, rl = oracle.attention(q, k, v, rows=rows)
     _cmp(o.reshape(-1, w.d)[rows], l.reshape(-1)[rows], ro, rl)
 
@@ -263,9 +271,12 @@ def test_rank_step_subrange():
     _cmp(o, l, ro, rl)
 
 
-def test_c5_full_size_sampled():
+def test_c5_full_size_every_tile():
     """One rank's 54,000 queries against 432,000 keys: per-step partials +
-    lse_merge (the benchmark's launch configuration) and the fused call."""
+    lse_merge (the benchmark's launch configuration) and the fused call, on
+    one row of every 128-row query tile of every head (1,688 rows, the lane
+    rotating over all 128 softmax threads) plus the chunk's first and last
+    rows."""
     w = synth.WORKLOADS["c5"]
     q, k, v = synth.make_qkv(w)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
@@ -274,8 +285,8 @@ def test_c5_full_size_sampled():
     fo, fl = ra.ring_attn_fwd_rank(qd, kd, vd, w.P, 0)
     torch.cuda.synchronize()
     assert ra.ra_get_status() == 0
-    per = synth.sample_rows(w, 12)
-    rows = oracle.flat_rows(w.B, w.H, w.L, per)
+    rows = np.unique(np.concatenate([synth.tile_rows(w.B * w.H, w.L, w.L),
+                                     oracle.flat_rows(w.B, w.H, w.L, synth.sample_rows(w, 12))]))
     ro, rl = oracle.attention(q, k, v, rows=rows)
     _cmp(o.reshape(-1, w.d)[rows.tolist()], l.reshape(-1)[rows.tolist()], ro, rl)
     _cmp(fo.reshape(-1, w.d)[rows.tolist()], fl.reshape(-1)[rows.tolist()], ro, rl)
@@ -360,10 +371,10 @@ def test_allgather_reducescatter_forms_match_oracle(form, B, H, S, d, P, causal)
 
 # ---------------------------------- every CP form at 14,400 tokens (sampled) --
 @pytest.mark.parametrize("form", ["overlap", "ulysses", "allgather", "reducescatter"])
-def test_cp_forms_c3_sampled_rows(form):
+def test_cp_forms_c3_every_tile(form):
     """The 14,400-token workload (3,600-row chunks: each rank's last 16 rows
     stacked into one tile) through every context-parallel form, on the rows
-    the ring test samples."""
+    the ring test checks (one per query tile, chunk and head)."""
     w = synth.WORKLOADS["c3"]
     q, k, v = synth.make_qkv(w)
     B, H, S, d, P = w.B, w.H, w.S, w.d, w.P
@@ -379,8 +390,7 @@ def test_cp_forms_c3_sampled_rows(form):
         l = l.cpu().permute(1, 2, 0, 3).reshape(B, H, S)
     torch.cuda.synchronize()
     assert ra.ra_get_status() == 0
-    per = synth.sample_rows(w, 48)
-    rows = oracle.flat_rows(B, H, S, per)
+    rows = _c3_rows(w)
     ro, rl = oracle.attention(q, k, v, rows=rows)
     _cmp(o.reshape(-1, d)[rows], l.reshape(-1)[rows], ro, rl)
 
@@ -408,19 +418,20 @@ def test_factored_small_full(B, H, T, N, d, P):
     _cmp(ot, lt, ro, rl)
 
 
-def test_factored_c4_sampled():
+def test_factored_c4_every_tile():
+    """48 frames x 900 tokens, H = 24: spatial output on one token of every
+    128-row query tile of every frame and head (9,216 rows, lanes rotating);
+    temporal output on every token (all 5,400 packed tiles per call)."""
     w = synth.WORKLOADS["c4"]
     q, k, v = synth.make_qkv(w)
     os_, ls, ot, lt = ra.factored_attn(q.cuda(), k.cuda(), v.cuda(), w.T, w.N, w.P)
     torch.cuda.synchronize()
     assert ra.ra_get_status() == 0
-    rng = np.random.default_rng(1003)
-    per = np.unique(np.concatenate([[0, w.S - 1, w.N - 1, w.N], rng.integers(0, w.S, 60)]))
-    rows = oracle.flat_rows(w.B, w.H, w.S, per)
+    rows = synth.tile_rows(w.B * w.H * w.T, w.N, w.N)
     ro, rl = oracle.factored(q, k, v, w.T, w.N, "spatial", rows=rows)
     _cmp(os_.reshape(-1, w.d)[rows.tolist()], ls.reshape(-1)[rows.tolist()], ro, rl)
-    ro, rl = oracle.factored(q, k, v, w.T, w.N, "temporal", rows=rows)
-    _cmp(ot.reshape(-1, w.d)[rows.tolist()], lt.reshape(-1)[rows.tolist()], ro, rl)
+    ro, rl = oracle.factored(q, k, v, w.T, w.N, "temporal")
+    _cmp(ot, lt, ro, rl)
 
 
 # ---------------------------------------------------------- edge + status --

@@ -29,7 +29,8 @@ def test_ring_schedule_matches_diagram():
 
 @pytest.mark.parametrize("P", [1, 2, 4, 8])
 def test_every_rank_sees_every_block_once(P):
-    """After P steps every query has seen every K/V block (day 83 blog)."""
+    """P steps bring each block to each rank exactly once (day 83 blog, "Context
+    parallelism: splitting the sequence")."""
     for r in range(P):
         assert sorted(oracle.ring_source(P, r, s) for s in range(P)) == list(range(P))
     # rank 0 of an 8-way ring visits 0, 7, 6, ..., 1
