@@ -616,13 +616,6 @@ size_t factored_attn_workspace(int B, int H, int T, int N, int d) {
   return T > kPackMaxFrames ? 4 * ws_part(rows * d * 2) + ws_part(rows * 4) : 0;
 }
 
-// Scratch a factored_attn call with this P actually uses: none while each
-// rank chunk (T / P frames) fits one tile, else the full position-major set.
-size_t ra::factored_scratch_bytes(int B, int H, int T, int N, int d, int P) {
-  if (P > 0 && T >= 0 && T % P == 0 && T / P <= kPackMaxFrames) return 0;
-  return factored_attn_workspace(B, H, T, N, d);
-}
-
 int factored_attn(const void *q, const void *k, const void *v, void *out_s, float *lse_s,
                   void *out_t, float *lse_t, int B, int H, int T, int N, int d, int P,
                   void *workspace, size_t ws_bytes, void *stream) {
@@ -777,3 +770,10 @@ int ra_watchdog_selftest(void *stream) {
 }
 
 }  // extern "C"
+
+// Scratch a factored_attn call with this P actually uses: none while each
+// rank chunk (T / P frames) fits one tile, else the full position-major set.
+size_t ra::factored_scratch_bytes(int B, int H, int T, int N, int d, int P) {
+  if (P > 0 && T >= 0 && T % P == 0 && T / P <= kPackMaxFrames) return 0;
+  return factored_attn_workspace(B, H, T, N, d);
+}
