@@ -42,6 +42,7 @@ extern "C" {
 #define RA_ERR_CUDA (-4)    /* a CUDA call or launch failed: see ra_last_cuda_error */
 #define RA_ERR_TIMEOUT (-5) /* a kernel's bounded wait expired (device watchdog)   */
 #define RA_ERR_WORKSPACE (-6) /* workspace missing or smaller than required        */
+#define RA_ERR_BOUNDS (-7)  /* a device index fell outside its buffer (RA_CHECKS build) */
 
 #define RA_LAYOUT_CONTIGUOUS 0
 #define RA_LAYOUT_ZIGZAG 1
@@ -278,18 +279,42 @@ int factored_attn_static(const void *q, const void *k, const void *v, void *out_
 
 /* Synchronises `stream`, then returns and clears the device status word:
  * RA_OK, or RA_ERR_TIMEOUT if a kernel's bounded wait expired since the last
- * call (the kernel then stopped early and its outputs are undefined), or
- * RA_ERR_CUDA if the synchronisation failed. */
+ * call (the kernel then stopped early and its outputs are undefined),
+ * RA_ERR_BOUNDS (checked builds only, see below), or RA_ERR_CUDA if the
+ * synchronisation failed. */
 int ra_get_status(void *stream);
 
 /* Bounded-wait limit of the kernels' barrier waits, in nanoseconds (default
  * 2e9).  Values <= 0 restore the default.  Applies to later launches. */
 void ra_set_watchdog_ns(int64_t ns);
 
+/* Folding of factored_attn's temporal ring (process-wide, later calls):
+ * 1 (default) lets adjacent rank chunks of at most 32 frames together share
+ * a block, so the ring has fewer, longer steps (12-frame chunks at P = 4 run
+ * as 2 blocks of 24 frames); 0 runs the ring over the P chunks exactly as
+ * given (P steps).  Both give the same result up to rounding order. */
+void ra_set_temporal_fold(int enable);
+
 /* Runs a kernel whose only wait can never be satisfied, with the current
  * watchdog limit, to exercise the timeout path: returns RA_OK when launched;
  * ra_get_status then reports RA_ERR_TIMEOUT. */
 int ra_watchdog_selftest(void *stream);
+
+/* Bounds-checked builds.  Compiled with -DRA_CHECKS, every kernel checks each
+ * global row index and TMA coordinate it computes against the extent of the
+ * buffer it addresses, and each TMEM column range against the allocation.
+ * A failed check records RA_ERR_BOUNDS in the device status word (read with
+ * ra_get_status; the first error since the last read wins) and the access is
+ * not made: a store is skipped, a TMA load is redirected to coordinate 0 so
+ * that its barrier still completes.  Outputs are then undefined.  The default
+ * build compiles no checks in and never reports RA_ERR_BOUNDS.
+ * ra_checks_enabled: 1 in a build with the checks, 0 otherwise.
+ * ra_checks_selftest: launches a kernel that checks one index against a bound
+ * it exceeds, without any memory access through that index; returns RA_OK
+ * when launched, after which ra_get_status reports RA_ERR_BOUNDS in a checked
+ * build and RA_OK in the default build. */
+int ra_checks_enabled(void);
+int ra_checks_selftest(void *stream);
 
 /* Text for an RA_* code; the last CUDA error (cudaError_t) seen on RA_ERR_CUDA. */
 const char *ra_strerror(int code);

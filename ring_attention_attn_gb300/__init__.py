@@ -22,8 +22,11 @@ from ._abi import (  # noqa: F401
     ra_get_status,
     ra_ring_source,
     ra_set_watchdog_ns,
+    ra_set_temporal_fold,
     ra_ulysses_a2a,
     ra_watchdog_selftest,
+    ra_checks_enabled,
+    ra_checks_selftest,
     ring_attn_fwd,
     ring_attn_bwd,
     ring_attn_bwd_workspace,

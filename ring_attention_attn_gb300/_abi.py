@@ -19,7 +19,7 @@ LIB_PATH = os.environ.get("RINGATTN_LIB") or os.path.join(HERE, "libringattn.so"
 
 RA_OK = 0
 ERRORS = {-1: "RA_ERR_ARG", -2: "RA_ERR_SHAPE", -3: "RA_ERR_ALIGN", -4: "RA_ERR_CUDA",
-          -5: "RA_ERR_TIMEOUT", -6: "RA_ERR_WORKSPACE"}
+          -5: "RA_ERR_TIMEOUT", -6: "RA_ERR_WORKSPACE", -7: "RA_ERR_BOUNDS"}
 
 # Every symbol include/ringattn.h declares.
 EXPORTS = ("ra_cp_shard_index", "ra_ring_source", "ra_cp_shard", "ra_frame_transpose",
@@ -29,8 +29,9 @@ EXPORTS = ("ra_cp_shard_index", "ra_ring_source", "ra_cp_shard", "ra_frame_trans
            "cp_allgather_attn_fwd", "cp_reducescatter_attn_fwd", "cp_variant_workspace",
            "lse_merge", "factored_attn",
            "factored_attn_workspace", "factored_attn_static", "ra_get_status",
-           "ra_set_watchdog_ns",
-           "ra_watchdog_selftest", "ra_strerror", "ra_last_cuda_error")
+           "ra_set_watchdog_ns", "ra_set_temporal_fold",
+           "ra_watchdog_selftest", "ra_checks_enabled", "ra_checks_selftest", "ra_strerror",
+           "ra_last_cuda_error")
 
 _lock = threading.Lock()
 _lib = None
@@ -87,7 +88,10 @@ def lib():
                                                i32, i32, vp]),
                 "ra_get_status": (i32, [vp]),
                 "ra_set_watchdog_ns": (None, [i64]),
+                "ra_set_temporal_fold": (None, [i32]),
                 "ra_watchdog_selftest": (i32, [vp]),
+                "ra_checks_enabled": (i32, []),
+                "ra_checks_selftest": (i32, [vp]),
                 "ra_strerror": (ctypes.c_char_p, [i32]),
                 "ra_last_cuda_error": (i32, []),
             }
@@ -392,5 +396,19 @@ def ra_set_watchdog_ns(ns: int):
     lib().ra_set_watchdog_ns(int(ns))
 
 
+def ra_set_temporal_fold(enable: bool):
+    """Fold short adjacent temporal chunks into fewer ring blocks (default on)."""
+    lib().ra_set_temporal_fold(int(bool(enable)))
+
+
 def ra_watchdog_selftest(stream=None):
     _check(lib().ra_watchdog_selftest(_stream(stream)), "ra_watchdog_selftest")
+
+
+def ra_checks_enabled() -> bool:
+    """True when the loaded library was built with the device bounds checks."""
+    return bool(lib().ra_checks_enabled())
+
+
+def ra_checks_selftest(stream=None):
+    _check(lib().ra_checks_selftest(_stream(stream)), "ra_checks_selftest")

@@ -2,6 +2,11 @@
 
 Each .cu translation unit compiles in parallel; the objects link into one
 shared library next to this file.  Usage: ``python -m ring_attention_attn_gb300.build``.
+``--checks`` builds the bounds-checked variant (``-DRA_CHECKS``: every kernel
+checks the global row indices, TMA coordinates and TMEM columns it computes
+and reports RA_ERR_BOUNDS instead of making an out-of-range access) into
+``libringattn_checks.so``, with its objects in a build folder of its own;
+load it through the RINGATTN_LIB environment variable.
 """
 from __future__ import annotations
 
@@ -16,6 +21,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libringattn.so")
+BUILD_CHECKS = os.path.join(HERE, "_build_checks")
+LIB_CHECKS = os.path.join(HERE, "libringattn_checks.so")
 SOURCES = ["api.cu", "attn_bwd.cu", "attn_fwd.cu", "merge.cu", "noalloc.cu", "shard.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -27,9 +34,11 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _flags(verbose_ptxas: bool):
+def _flags(verbose_ptxas: bool, checks: bool = False):
     f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                 "-I", os.path.join(ROOT, "include"), "-I", CSRC]
+    if checks:
+        f += ["-DRA_CHECKS"]
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]
     return f
@@ -42,14 +51,16 @@ def _newer(target: str, deps) -> bool:
     return all(os.path.getmtime(d) <= t for d in deps)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None,
+          checks: bool = False) -> str:
+    build_dir, lib_path = (BUILD_CHECKS, LIB_CHECKS) if checks else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".cuh", ".h"))]
     headers.append(os.path.join(ROOT, "include", "ringattn.h"))
     objs, todo = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src[:-3] + ".o")
+        o = os.path.join(build_dir, src[:-3] + ".o")
         objs.append(o)
         if force or verbose_ptxas or not _newer(o, [s] + headers):
             todo.append((s, o))
@@ -57,7 +68,7 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
 
     def compile_one(so):
         s, o = so
-        cmd = [cc] + _flags(verbose_ptxas) + ["-c", s, "-o", o]
+        cmd = [cc] + _flags(verbose_ptxas, checks) + ["-c", s, "-o", o]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return s, r
 
@@ -68,17 +79,17 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
                     sys.stderr.write(r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError(f"nvcc failed on {os.path.basename(s)}")
-    if todo or not _newer(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if todo or not _newer(lib_path, objs):
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("link failed")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv,
+                checks="--checks" in sys.argv))

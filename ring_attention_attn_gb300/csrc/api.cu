@@ -16,6 +16,7 @@ __device__ int g_status;  // first device-side error since the last ra_get_statu
 
 std::atomic<int> g_last_cuda_error{0};
 std::atomic<int64_t> g_watchdog_ns{2000000000LL};
+std::atomic<int> g_temporal_fold{1};
 
 int fail_cuda(cudaError_t e) {
   g_last_cuda_error.store(static_cast<int>(e));
@@ -83,6 +84,8 @@ const char *ra_strerror(int code) {
     case RA_ERR_CUDA: return "CUDA error (see ra_last_cuda_error)";
     case RA_ERR_TIMEOUT: return "device watchdog: a kernel's bounded wait expired";
     case RA_ERR_WORKSPACE: return "workspace missing or too small";
+    case RA_ERR_BOUNDS:
+      return "bounds check (RA_CHECKS build): a device index fell outside its buffer";
     default: return "unknown error";
   }
 }
@@ -90,6 +93,8 @@ const char *ra_strerror(int code) {
 int ra_last_cuda_error(void) { return g_last_cuda_error.load(); }
 
 void ra_set_watchdog_ns(int64_t ns) { g_watchdog_ns.store(ns > 0 ? ns : 2000000000LL); }
+
+void ra_set_temporal_fold(int enable) { g_temporal_fold.store(enable != 0 ? 1 : 0); }
 
 int ra_cp_shard_index(int64_t S, int P, int layout, int64_t *s2g, int64_t *g2s) {
   if (S < 0 || P <= 0 || (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG))
@@ -124,7 +129,7 @@ int ra_cp_shard(const void *x, void *y, int64_t BH, int64_t S, int d, int P, int
   if (!x || !y) return RA_ERR_ARG;
   if (!aligned16(x) || !aligned16(y)) return RA_ERR_ALIGN;
   if (BH * S > kMaxRows) return RA_ERR_SHAPE;
-  cudaError_t e = ra::launch_row_permute(x, y, BH, S, d * 2, inverse ? 1 : 0, P, 0, layout,
+  cudaError_t e = ra::launch_row_permute(x, y, BH, S, d * 2, inverse ? 1 : 0, P, 0, layout, status_ptr(),
                                          as_stream(stream));
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
@@ -137,7 +142,7 @@ int ra_frame_transpose(const void *x, void *y, int64_t BH, int64_t T, int64_t N,
   if (!x || !y) return RA_ERR_ARG;
   if (!aligned16(x) || !aligned16(y)) return RA_ERR_ALIGN;
   if (BH * T * N > kMaxRows) return RA_ERR_SHAPE;
-  cudaError_t e = ra::launch_row_permute(x, y, BH, T * N, d * 2, inverse ? 3 : 2, T, N, 0,
+  cudaError_t e = ra::launch_row_permute(x, y, BH, T * N, d * 2, inverse ? 3 : 2, T, N, 0, status_ptr(),
                                          as_stream(stream));
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
@@ -344,7 +349,7 @@ int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out
     if (e == cudaSuccess && s >= 1) e = cudaEventRecord(consumed[s & 1], cs);
   }
   if (e == cudaSuccess)
-    e = ra::launch_lse_merge(o_parts, l_parts, P, BH * S, d, out, lse, cs);
+    e = ra::launch_lse_merge(o_parts, l_parts, P, BH * S, d, out, lse, status_ptr(), cs);
   for (int i = 0; i < 2; ++i) {
     cudaEventDestroy(copied[i]);
     cudaEventDestroy(consumed[i]);
@@ -362,7 +367,7 @@ int ra_ulysses_a2a(const void *x, void *y, int B, int H, int64_t S, int d, int P
   if (!x || !y) return RA_ERR_ARG;
   if (!aligned16(x) || !aligned16(y)) return RA_ERR_ALIGN;
   if (BH * S > kMaxRows) return RA_ERR_SHAPE;
-  cudaError_t e = ra::launch_row_permute(x, y, BH, S, d * 2, inverse ? 5 : 4, P, H, B,
+  cudaError_t e = ra::launch_row_permute(x, y, BH, S, d * 2, inverse ? 5 : 4, P, H, B, status_ptr(),
                                          as_stream(stream));
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
@@ -398,7 +403,7 @@ int ulysses_attn_fwd(const void *q, const void *k, const void *v, void *out, flo
   void *dst[3] = {qh, kh, vh};
   cudaError_t e;
   for (int i = 0; i < 3; ++i) {
-    e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 4, P, H, B, st);
+    e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 4, P, H, B, status_ptr(), st);
     if (e != cudaSuccess) return fail_cuda(e);
   }
   // Head-split: B*H heads of S tokens in global order; no ring (P = 1).
@@ -420,9 +425,9 @@ int ulysses_attn_fwd(const void *q, const void *k, const void *v, void *out, flo
   p.wd = wd;
   e = ra::launch_ring_attn(qh, BH * S, kh, vh, BH * S, d, false, p, st);
   if (e != cudaSuccess) return fail_cuda(e);
-  e = ra::launch_row_permute(oh, out, BH, S, d * 2, 5, P, H, B, st);
+  e = ra::launch_row_permute(oh, out, BH, S, d * 2, 5, P, H, B, status_ptr(), st);
   if (e != cudaSuccess) return fail_cuda(e);
-  e = ra::launch_row_permute(lh, lse, BH, S, 4, 5, P, H, B, st);
+  e = ra::launch_row_permute(lh, lse, BH, S, 4, 5, P, H, B, status_ptr(), st);
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
 
@@ -466,8 +471,8 @@ int cp_allgather_attn_fwd(const void *q, const void *k, const void *v, void *out
   const size_t tb = ovl_part(static_cast<size_t>(BH * S) * d * 2);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   void *kg = ws + tb, *vg = ws + 2 * tb;
-  cudaError_t e = ra::launch_row_permute(k, kg, BH, S, d * 2, 6, P, H, B, st);
-  if (e == cudaSuccess) e = ra::launch_row_permute(v, vg, BH, S, d * 2, 6, P, H, B, st);
+  cudaError_t e = ra::launch_row_permute(k, kg, BH, S, d * 2, 6, P, H, B, status_ptr(), st);
+  if (e == cudaSuccess) e = ra::launch_row_permute(v, vg, BH, S, d * 2, 6, P, H, B, status_ptr(), st);
   if (e == cudaSuccess) {
     // Every rank's own queries (buffer r) against every block of the gathered
     // K/V, all ranks in one launch.
@@ -516,7 +521,7 @@ int cp_reducescatter_attn_fwd(const void *q, const void *k, const void *v, void 
   void *dst[3] = {qg, kg, vg};
   cudaError_t e = cudaSuccess;
   for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-    e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 6, P, H, B, st);
+    e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 6, P, H, B, status_ptr(), st);
   if (e == cudaSuccess) {
     // Every (rank, block) pair once; the partial is filed under the block.
     ra::AttnParams p{};
@@ -543,9 +548,9 @@ int cp_reducescatter_attn_fwd(const void *q, const void *k, const void *v, void 
     p.wd = wd;
     e = ra::launch_ring_attn(qg, BH * S, kg, vg, BH * S, d, true, p, st);
   }
-  if (e == cudaSuccess) e = ra::launch_lse_merge(o_parts, l_parts, P, BH * S, d, og, lg, st);
-  if (e == cudaSuccess) e = ra::launch_row_permute(og, out, BH, S, d * 2, 7, P, H, B, st);
-  if (e == cudaSuccess) e = ra::launch_row_permute(lg, lse, BH, S, 4, 7, P, H, B, st);
+  if (e == cudaSuccess) e = ra::launch_lse_merge(o_parts, l_parts, P, BH * S, d, og, lg, status_ptr(), st);
+  if (e == cudaSuccess) e = ra::launch_row_permute(og, out, BH, S, d * 2, 7, P, H, B, status_ptr(), st);
+  if (e == cudaSuccess) e = ra::launch_row_permute(lg, lse, BH, S, 4, 7, P, H, B, status_ptr(), st);
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
 
@@ -596,7 +601,7 @@ int lse_merge(const float *o_parts, const float *lse_parts, int n, int64_t rows,
   if (!o_parts || !lse_parts || !out || !lse_out) return RA_ERR_ARG;
   if (!aligned16(o_parts) || !aligned16(out) || !aligned16(lse_parts) || !aligned16(lse_out))
     return RA_ERR_ALIGN;
-  cudaError_t e = ra::launch_lse_merge(o_parts, lse_parts, n, rows, d, out, lse_out,
+  cudaError_t e = ra::launch_lse_merge(o_parts, lse_parts, n, rows, d, out, lse_out, status_ptr(),
                                        as_stream(stream));
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
@@ -678,7 +683,7 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
     void *dst[3] = {ws + tbytes, ws + 2 * tbytes, ws + 3 * tbytes};
     const void *src[3] = {q, k, v};
     for (int i = 0; i < 3; ++i) {
-      e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 2, T, N, 0, st);
+      e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 2, T, N, 0, status_ptr(), st);
       if (e != cudaSuccess) return fail_cuda(e);
     }
     tq = dst[0];
@@ -696,7 +701,7 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
     // warp-packed tiles) and keeps at least two blocks (a CTA's two query
     // tiles): 12-frame chunks at P = 4 fold in pairs.
     int f = 1;
-    if (packed)
+    if (packed && g_temporal_fold.load())
       for (int c = 2; c <= P / 2; ++c)
         if (P % c == 0 && static_cast<int64_t>(c) * (T / P) <= 32) f = c;
     const int Pr = P / f;  // ring size after folding
@@ -742,9 +747,9 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
     if (e != cudaSuccess) return fail_cuda(e);
   }
   if (!packed) {
-    e = ra::launch_row_permute(oT, out_t, BH, S, d * 2, 3, T, N, 0, st);
+    e = ra::launch_row_permute(oT, out_t, BH, S, d * 2, 3, T, N, 0, status_ptr(), st);
     if (e != cudaSuccess) return fail_cuda(e);
-    e = ra::launch_row_permute(lT, lse_t, BH, S, 4, 3, T, N, 0, st);
+    e = ra::launch_row_permute(lT, lse_t, BH, S, 4, 3, T, N, 0, status_ptr(), st);
     if (e != cudaSuccess) return fail_cuda(e);
   }
   return RA_OK;
@@ -760,6 +765,21 @@ int ra_get_status(void *stream) {
   e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
   if (e != cudaSuccess) return fail_cuda(e);
   return v;
+}
+
+int ra_checks_enabled(void) {
+#ifdef RA_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int ra_checks_selftest(void *stream) {
+  int *st = status_ptr();
+  if (st == nullptr) return fail_cuda(cudaGetLastError());
+  cudaError_t e = ra::launch_checks_selftest(st, as_stream(stream));
+  return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
 
 int ra_watchdog_selftest(void *stream) {

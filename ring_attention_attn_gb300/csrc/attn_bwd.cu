@@ -221,6 +221,7 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUten
     bh = u / p.P;
   }
   const int64_t C2 = p.L >> 1;
+  const int64_t n_rows = static_cast<int64_t>(p.BH) * p.S;  // rows of every [BH, S] tensor
   const int64_t q0 = static_cast<int64_t>(qt) * 128;
   const int64_t nq = stacked ? static_cast<int64_t>(p.P) * p.rem : min64(128, p.L - q0);
   const int64_t q_row0 = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(r) * p.L + q0;
@@ -260,7 +261,8 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUten
         // the 128-byte swizzle phase).
         mbar_arrive_expect_tx(bb.b(kBA), static_cast<uint32_t>(2 * p.P * p.rem * 128 * C::kChunks));
         for (int rr = 0; rr < p.P; ++rr) {
-          const int32_t y = static_cast<int32_t>(q_row0 + static_cast<int64_t>(rr) * p.L);
+          int32_t y = static_cast<int32_t>(q_row0 + static_cast<int64_t>(rr) * p.L);
+          if (!RA_IN_BOUNDS(y >= 0 && static_cast<int64_t>(y) + p.rem <= n_rows, wd.status)) y = 0;
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c) {
             tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes + rr * p.rem * 128, &tm_qr, c * 64, y,
@@ -270,21 +272,22 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUten
           }
         }
       } else {
+        int32_t y = static_cast<int32_t>(q_row0);
+        if (!RA_IN_BOUNDS(q_row0 >= 0 && q_row0 < n_rows, wd.status)) y = 0;
         mbar_arrive_expect_tx(bb.b(kBA), 2 * C::kTile);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes, &tm_q, c * 64,
-                      static_cast<int32_t>(q_row0), bb.b(kBA));
-          tma_load_2d(sbase + C::kOffB + c * C::kChunkBytes, &tm_do, c * 64,
-                      static_cast<int32_t>(q_row0), bb.b(kBA));
+          tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes, &tm_q, c * 64, y, bb.b(kBA));
+          tma_load_2d(sbase + C::kOffB + c * C::kChunkBytes, &tm_do, c * 64, y, bb.b(kBA));
         }
       }
       int it = 0;
       bool ok = true;
       for (auto ti = make_iter(); ok && ti.valid(); ++ti.t, ti.settle()) {
-        const int32_t ky = static_cast<int32_t>(static_cast<int64_t>(bh) * p.S +
-                                                static_cast<int64_t>(ti.blk) * p.L +
-                                                static_cast<int64_t>(ti.t) * 128);
+        int32_t ky = static_cast<int32_t>(static_cast<int64_t>(bh) * p.S +
+                                          static_cast<int64_t>(ti.blk) * p.L +
+                                          static_cast<int64_t>(ti.t) * 128);
+        if (!RA_IN_BOUNDS(ky >= 0 && ky < n_rows, wd.status)) ky = 0;
         for (int which = 0; which < 2 && ok; ++which, ++it) {
           const int slot = it % C::kSlots;
           if (!(ok = mbar_wait(bb.kv_empty0 + 8 * slot, ((it / C::kSlots) & 1) ^ 1, wd, abort_flag)))
@@ -373,9 +376,12 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUten
     const int row = quarter * 32 + lane;
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_bits + kColS + 64 * h, tP = tmem + lane_bits + kColP + 64 * h;
-    const bool valid = row < nq;
     const int64_t grow =
         stacked ? q_row0 + static_cast<int64_t>(row / p.rem) * p.L + row % p.rem : q_row0 + row;
+    const bool valid =
+        row < nq && RA_IN_BOUNDS(grow >= 0 && grow < n_rows && (D / 2) * h + D / 2 <= D &&
+                                     kColQT + (D / 2) * (h + 1) <= 512,
+                                 wd.status);
     const float lse2 = valid ? p.lse[grow] * kLog2eB : 0.f;
     const float Drow = valid ? p.Dv[grow] : 0.f;
     const int64_t gq = CAUSAL ? zz_pos(r, min64(q0 + row, p.L - 1), C2, p.P) : 0;
@@ -504,6 +510,7 @@ __device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUte
     bh = u / p.P;
   }
   const int64_t C2 = p.L >> 1;
+  const int64_t n_rows = static_cast<int64_t>(p.BH) * p.S;  // rows of every [BH, S] tensor
   const int64_t k0 = static_cast<int64_t>(kt) * 128;
   const int64_t nk = stacked ? static_cast<int64_t>(p.P) * p.rem : min64(128, p.L - k0);
   const int64_t k_row0 = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(b) * p.L + k0;
@@ -542,7 +549,8 @@ __device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUte
       if (stacked) {
         mbar_arrive_expect_tx(bb.b(kBA), static_cast<uint32_t>(2 * p.P * p.rem * 128 * C::kChunks));
         for (int rr = 0; rr < p.P; ++rr) {
-          const int32_t y = static_cast<int32_t>(k_row0 + static_cast<int64_t>(rr) * p.L);
+          int32_t y = static_cast<int32_t>(k_row0 + static_cast<int64_t>(rr) * p.L);
+          if (!RA_IN_BOUNDS(y >= 0 && static_cast<int64_t>(y) + p.rem <= n_rows, wd.status)) y = 0;
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c) {
             tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes + rr * p.rem * 128, &tm_kr, c * 64, y,
@@ -552,21 +560,22 @@ __device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUte
           }
         }
       } else {
+        int32_t y = static_cast<int32_t>(k_row0);
+        if (!RA_IN_BOUNDS(k_row0 >= 0 && k_row0 < n_rows, wd.status)) y = 0;
         mbar_arrive_expect_tx(bb.b(kBA), 2 * C::kTile);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes, &tm_k, c * 64,
-                      static_cast<int32_t>(k_row0), bb.b(kBA));
-          tma_load_2d(sbase + C::kOffB + c * C::kChunkBytes, &tm_v, c * 64,
-                      static_cast<int32_t>(k_row0), bb.b(kBA));
+          tma_load_2d(sbase + C::kOffA + c * C::kChunkBytes, &tm_k, c * 64, y, bb.b(kBA));
+          tma_load_2d(sbase + C::kOffB + c * C::kChunkBytes, &tm_v, c * 64, y, bb.b(kBA));
         }
       }
       int it = 0;
       bool ok = true;
       for (auto ti = make_iter(); ok && ti.valid(); ++ti.t, ti.settle()) {
-        const int32_t qy = static_cast<int32_t>(static_cast<int64_t>(bh) * p.S +
-                                                static_cast<int64_t>(ti.blk) * p.L +
-                                                static_cast<int64_t>(ti.t) * 128);
+        int32_t qy = static_cast<int32_t>(static_cast<int64_t>(bh) * p.S +
+                                          static_cast<int64_t>(ti.blk) * p.L +
+                                          static_cast<int64_t>(ti.t) * 128);
+        if (!RA_IN_BOUNDS(qy >= 0 && qy < n_rows, wd.status)) qy = 0;
         for (int which = 0; which < 2 && ok; ++which, ++it) {
           const int slot = it % C::kSlots;
           if (!(ok = mbar_wait(bb.kv_empty0 + 8 * slot, ((it / C::kSlots) & 1) ^ 1, wd, abort_flag)))
@@ -672,6 +681,7 @@ __device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUte
       if (64 * h + qi >= min64(128, p.L - tq0)) return 0.f;
       const int64_t qrow = static_cast<int64_t>(bh) * p.S + static_cast<int64_t>(t.blk) * p.L +
                            tq0 + 64 * h + qi;
+      if (!RA_IN_BOUNDS(qrow >= 0 && qrow < n_rows, wd.status)) return 0.f;
       return row < 64 ? -(p.lse[qrow] * kLog2eB) : -p.Dv[qrow];
     };
     int j = 0;
@@ -747,6 +757,7 @@ __device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUte
       // Warpgroup 0 writes the dV row, warpgroup 1 the dK row.
       const int64_t grow =
           stacked ? k_row0 + static_cast<int64_t>(row / p.rem) * p.L + row % p.rem : k_row0 + row;
+      const bool store = kvalid && RA_IN_BOUNDS(grow >= 0 && grow < n_rows, wd.status);
       const uint32_t tA = tmem + lane_bits + (h == 0 ? kColAcc0 : kColAcc1);
       __nv_bfloat16 *dst = (h == 0 ? p.dv : p.dk) + grow * D;
       const float mul = h == 0 ? 1.f : p.scale;
@@ -760,7 +771,7 @@ __device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUte
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] = 0.f;
         }
-        if (kvalid) store_row_bf16(dst + c * 32, o, mul);
+        if (store) store_row_bf16(dst + c * 32, o, mul);
       }
     }
   }

@@ -312,16 +312,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Packed mode: box {64 d, Lf frames, pack positions, 1 head} of the
         // [head][frame][position][d] tensor, starting at the rank's first
         // frame and the unit's first position.
-        const int32_t pn = w.g * p.pack;
+        int32_t pn = w.g * p.pack;
+        int32_t pbh = w.bh;
         if (kPack) {
+          int32_t f0 = w.rank * p.Lf, f1 = (w.rank + 1) * p.Lf;
+          if (!RA_IN_BOUNDS(pn >= 0 && pn < p.pN && pbh >= 0 && pbh < p.BH && f0 >= 0 &&
+                                f0 < p.pT && (!g.has_q1 || f1 < p.pT),
+                            wd.status))
+            pn = pbh = f0 = f1 = 0;
           mbar_arrive_expect_tx(qfull, g.has_q1 ? 2 * pack_bytes : pack_bytes);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_4d(sbase + C::kOffQ0 + c * C::kChunkBytes, &tm_q, c * 64, w.rank * p.Lf, pn,
-                        w.bh, qfull);
+            tma_load_4d(sbase + C::kOffQ0 + c * C::kChunkBytes, &tm_q, c * 64, f0, pn, pbh, qfull);
             if (g.has_q1)
-              tma_load_4d(sbase + C::kOffQ1 + c * C::kChunkBytes, &tm_q, c * 64,
-                          (w.rank + 1) * p.Lf, pn, w.bh, qfull);
+              tma_load_4d(sbase + C::kOffQ1 + c * C::kChunkBytes, &tm_q, c * 64, f1, pn, pbh,
+                          qfull);
           }
         } else if (kRem && w.rem) {
           // rem_pack rows of each rank, stacked in the first query tile
@@ -330,14 +335,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t rstride = p.q_rank_stride ? p.q_rank_stride : p.L;
           mbar_arrive_expect_tx(qfull, static_cast<uint32_t>(p.n_ranks * rr * 128 * C::kChunks));
           for (int r = 0; r < p.n_ranks; ++r) {
-            const int32_t qy = static_cast<int32_t>(w.q_row0 + r * rstride + g.pair_row0);
+            int32_t qy = static_cast<int32_t>(w.q_row0 + r * rstride + g.pair_row0);
+            if (!RA_IN_BOUNDS(qy >= 0 && static_cast<int64_t>(qy) + rr <= p.chk_q_rows,
+                              wd.status))
+              qy = 0;
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
               tma_load_2d(sbase + C::kOffQ0 + c * C::kChunkBytes + r * rr * 128, &tm_qr, c * 64, qy,
                           qfull);
           }
         } else {
-          const int32_t qy = static_cast<int32_t>(w.q_row0 + g.pair_row0);
+          int32_t qy = static_cast<int32_t>(w.q_row0 + g.pair_row0);
+          if (!RA_IN_BOUNDS(qy >= 0 && qy < p.chk_q_rows &&
+                                (!g.has_q1 || static_cast<int64_t>(qy) + kBM < p.chk_q_rows),
+                            wd.status))
+            qy = 0;
           mbar_arrive_expect_tx(qfull, 2 * C::kQTile);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c) {
@@ -352,7 +364,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t blk = p.kv_own ? static_cast<int64_t>(w.rank) * p.kv_rank_stride +
                                              static_cast<int64_t>(w.bh) * p.kv_rows_bh
                                        : kv_base + static_cast<int64_t>(ti.src) * p.L;
-          const int32_t ky = static_cast<int32_t>(blk + static_cast<int64_t>(ti.t) * kBN);
+          int32_t ky = static_cast<int32_t>(blk + static_cast<int64_t>(ti.t) * kBN);
+          int32_t kf = ti.src * p.Lf;
+          if (!RA_IN_BOUNDS(kPack ? (kf >= 0 && kf < p.pT) : (ky >= 0 && ky < p.chk_kv_rows),
+                            wd.status))
+            ky = kf = 0;
 #pragma unroll
           for (int which = 0; which < 2; ++which) {
             const int slot = it % C::kSlots;
@@ -367,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int c = 0; c < C::kChunks; ++c)
                 tma_load_4d(sbase + C::kOffKV + slot * C::kKVTile + c * C::kChunkBytes, map,
-                            c * 64, ti.src * p.Lf, pn, w.bh, kv_full0 + 8 * slot);
+                            c * 64, kf, pn, pbh, kv_full0 + 8 * slot);
             } else {
               mbar_arrive_expect_tx(kv_full0 + 8 * slot, C::kKVTile);
 #pragma unroll
@@ -492,6 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_bits + col_s(wg);
     const uint32_t tO = tmem + lane_bits + col_o(wg);
+    // This thread's TMEM lanes and columns: its S tile and O accumulator.
+    (void)RA_IN_BOUNDS(wg < 2 && row < kBM && col_s(wg) + kBN <= kTmemCols &&
+                           col_o(wg) + D <= kTmemCols && (col_o(wg) >= col_s(1) + kBN),
+                       wd.status);
     const float sl2 = p.scale_log2;
     // Rows start 32-byte aligned when the output and its part stride are
     // (the entry points only promise 16): then 32-byte stores are used.
@@ -537,7 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int64_t gq = CAUSAL ? zz_pos(w.rank, min64(qi, p.L - 1), p.L >> 1, p.P) : 0;
 
-      float m_ref = -INFINITY, l = 0.f;
+      // l sums the probabilities as computed (it gives the LSE); packed tiles
+      // also sum them as rounded to bf16 (lr), the weights the PV MMA
+      // actually applies, and normalise O by that: rows of a few dozen keys,
+      // often dominated by one, would otherwise carry the rounding of the
+      // dominant probability (up to 2^-9 relative) straight into O.
+      float m_ref = -INFINITY, l = 0.f, lr = 0.f;
       int j = 0;
       TileIter ti;
       ti.init(p, w);
@@ -550,9 +575,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (PK == 2) {
           float alpha = 1.f;
           bool rescale = false;
-          float2 rs[4];
+          float2 rs[4], rq[4];
 #pragma unroll
-          for (int x = 0; x < 4; ++x) rs[x] = make_float2(0.f, 0.f);
+          for (int x = 0; x < 4; ++x) rs[x] = rq[x] = make_float2(0.f, 0.f);
           // Warp-packed temporal tiles: problems of pLrow = 16 or 32 rows sit
           // at the same offsets in the query and the key tile, so the keys
           // of this warp's 32 rows are exactly its own 32-column chunk: only
@@ -591,6 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 e = make_float2(ex2(a.x), ex2(a.y));
             rs[x & 3] = fadd2(rs[x & 3], e);
             pk[x] = pack_bf16x2(e.x, e.y);
+            rq[x & 3] = fadd2(rq[x & 3], unpack_bf16x2(pk[x]));
             zero[x] = 0u;
           }
 #pragma unroll
@@ -599,6 +625,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 r = fadd2(r01, r23);
           const float rsum = r.x + r.y;
           l = l * alpha + rsum;
+          const float2 q01 = fadd2(rq[0], rq[1]), q23 = fadd2(rq[2], rq[3]);
+          const float2 rqs = fadd2(q01, q23);
+          lr = lr * alpha + (rqs.x + rqs.y);
           if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -651,9 +680,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float shift = (m_ref == -INFINITY) ? 0.f : m_ref;
           const float2 sl2v = make_float2(sl2, sl2);
           const float2 nshift = make_float2(-shift, -shift);
-          float2 rs[4];
+          float2 rs[4], rq[4];
 #pragma unroll
-          for (int x = 0; x < 4; ++x) rs[x] = make_float2(0.f, 0.f);
+          for (int x = 0; x < 4; ++x) rs[x] = rq[x] = make_float2(0.f, 0.f);
           // P overwrites the first 64 columns of this tile's S (already in
           // registers): bf16 pairs, lower key in the low half.  Scale/shift and
           // the row sum use packed f32x2 arithmetic (two scores per instruction).
@@ -666,6 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float2 e = make_float2(ex2(a.x), ex2(a.y));
               rs[x & 3] = fadd2(rs[x & 3], e);
               pk[x] = pack_bf16x2(e.x, e.y);
+              if constexpr (kPack) rq[x & 3] = fadd2(rq[x & 3], unpack_bf16x2(pk[x]));
             }
             tmem_st16(tS + c * 16, pk);
           }
@@ -673,6 +703,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 r = fadd2(r01, r23);
           const float rsum = r.x + r.y;
           l = l * alpha + rsum;
+          if constexpr (kPack) {
+            const float2 q01 = fadd2(rq[0], rq[1]), q23 = fadd2(rq[2], rq[3]);
+            const float2 rqs = fadd2(q01, q23);
+            lr = lr * alpha + (rqs.x + rqs.y);
+          }
           if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -705,7 +740,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       jt += j;
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const float l_o = kPack ? lr : l;  // the normaliser of O
+      const float inv_l = (l_o > 0.f) ? 1.f / l_o : 0.f;
       const float lse_val = (l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
       const int part = p.part_by_block ? ((w.rank - w.s_lo) % p.P + p.P) % p.P : w.part;
       // Packed mode: frame f = (w.rank + wg) * Lf + qi % pLrow of position
@@ -716,6 +752,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           !kPack                 ? w.q_row0 + rem_off
           : p.pack_frame_major ? (static_cast<int64_t>(w.bh) * p.pT + pf) * p.pN + pn
                                : (static_cast<int64_t>(w.bh) * p.pN + pn) * p.pT + pf;
+      if (row_valid && !RA_IN_BOUNDS(orow >= 0 && orow < p.chk_out_rows && part >= 0 &&
+                                         part < p.chk_parts,
+                                     wd.status))
+        row_valid = false;
       if (OUT_F32) {
         float *out = reinterpret_cast<float *>(p.out) + part * p.out_part_stride + orow * D;
 #pragma unroll
@@ -810,6 +850,12 @@ __global__ void watchdog_selftest_kernel(WatchdogParams wdp) {
   const Watchdog wd{wdp.status, wdp.limit_ns};
   if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, wd, &abort_flag);
   __syncthreads();
+}
+
+// Checks one index against a bound it exceeds, touching no memory through
+// it: the RA_CHECKS build records RA_ERR_BOUNDS, the default build nothing.
+__global__ void checks_selftest_kernel(int *status, int index, int bound) {
+  (void)RA_IN_BOUNDS(index < bound, status);
 }
 
 // --------------------------------------------------------------- host side --
@@ -922,14 +968,23 @@ cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const C
 }  // namespace
 
 cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k, const void *v,
-                             int64_t kv_total_rows, int d, bool out_f32, const AttnParams &p,
-                             cudaStream_t stream) {
-  const int64_t per_pair = static_cast<int64_t>(p.BH) * p.G * p.n_stepgroups;
+                             int64_t kv_total_rows, int d, bool out_f32,
+                             const AttnParams &params, cudaStream_t stream) {
+  const int64_t per_pair = static_cast<int64_t>(params.BH) * params.G * params.n_stepgroups;
   // With rem_pack every rank's single last tile shares one unit.
-  const int64_t n_units = p.rem_pack > 0 ? per_pair * ((p.n_pairs - 1) * p.n_ranks + 1)
-                                         : per_pair * p.n_ranks * p.n_pairs;
+  const int64_t n_units =
+      params.rem_pack > 0 ? per_pair * ((params.n_pairs - 1) * params.n_ranks + 1)
+                          : per_pair * params.n_ranks * params.n_pairs;
   if (n_units <= 0) return cudaSuccess;
   if (n_units > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  // Extents the RA_CHECKS build checks indices against: outputs have as many
+  // rows per part as the Q row matrix, one part per step group (or per block).
+  AttnParams pc = params;
+  pc.chk_q_rows = q_total_rows;
+  pc.chk_kv_rows = kv_total_rows;
+  pc.chk_out_rows = q_total_rows;
+  pc.chk_parts = pc.part_by_block ? pc.P : pc.n_stepgroups;
+  const AttnParams &p = pc;
   CUtensorMap mq, mk, mv, mqr;
   cudaError_t e;
   if (p.pack) {
@@ -973,6 +1028,12 @@ cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k,
                    : launch_variant<64, false, 0, true>(mq, mk, mv, mqr, p, n_units, stream);
   return out_f32 ? launch_variant<64, true, 0, false>(mq, mk, mv, mqr, p, n_units, stream)
                  : launch_variant<64, false, 0, false>(mq, mk, mv, mqr, p, n_units, stream);
+}
+
+cudaError_t launch_checks_selftest(int *status, cudaStream_t stream) {
+  if (status == nullptr) return cudaErrorInvalidValue;
+  checks_selftest_kernel<<<1, 1, 0, stream>>>(status, 1, 1);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_watchdog_selftest(const WatchdogParams &wd, cudaStream_t stream) {

@@ -17,6 +17,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "ra_device.cuh"
 #include "ra_internal.h"
 
 namespace ra {
@@ -52,7 +53,8 @@ __global__ void __launch_bounds__(256) lse_merge_kernel8(const float *__restrict
                                                          const float *__restrict__ lse_parts,
                                                          int n, int64_t rows,
                                                          __nv_bfloat16 *__restrict__ out,
-                                                         float *__restrict__ lse_out) {
+                                                         float *__restrict__ lse_out,
+                                                         int *status) {
   constexpr int kLanes = D / 4;  // lanes per row
   constexpr int kRowsPerWarp = 32 / kLanes;
   const int lane = threadIdx.x & 31;
@@ -68,7 +70,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel8(const float *__restrict
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
       row[r] = base + r * kRowsPerWarp + lane / kLanes;
-      const bool ok = row[r] < rows;
+      const bool ok = row[r] < rows && RA_IN_BOUNDS(n <= 8 && sub < kLanes, status);
       const float4 *src = reinterpret_cast<const float4 *>(o_parts) + row[r] * kLanes + sub;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -117,14 +119,15 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float *__restrict_
                                                         const float *__restrict__ lse_parts,
                                                         int n, int64_t rows,
                                                         __nv_bfloat16 *__restrict__ out,
-                                                        float *__restrict__ lse_out) {
+                                                        float *__restrict__ lse_out,
+                                                        int *status) {
   constexpr int kLanes = D / 4;            // lanes per row
   constexpr int kRowsPerWarp = 32 / kLanes;
   const int lane = threadIdx.x & 31;
   const int sub = lane % kLanes;
   const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t row = warp_global * kRowsPerWarp + lane / kLanes;
-  if (row >= rows) return;
+  if (row >= rows || !RA_IN_BOUNDS(row >= 0 && sub < kLanes, status)) return;
 
   float M = -INFINITY;
   for (int i = 0; i < n; ++i) M = fmaxf(M, __ldg(lse_parts + static_cast<int64_t>(i) * rows + row));
@@ -170,8 +173,10 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float *__restrict_
 }  // namespace
 
 cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int n, int64_t rows,
-                             int d, void *out, float *lse_out, cudaStream_t stream) {
+                             int d, void *out, float *lse_out, int *status,
+                             cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
+  if (status == nullptr) return cudaErrorInvalidValue;
   if (n <= 8) {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess)
@@ -182,10 +187,10 @@ cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int n
     const int grid = static_cast<int>(want < sms * 8 ? want : sms * 8);
     if (d == 128)
       lse_merge_kernel8<128, kRows><<<grid, 256, 0, stream>>>(
-          o_parts, lse_parts, n, rows, static_cast<__nv_bfloat16 *>(out), lse_out);
+          o_parts, lse_parts, n, rows, static_cast<__nv_bfloat16 *>(out), lse_out, status);
     else
       lse_merge_kernel8<64, kRows><<<grid, 256, 0, stream>>>(
-          o_parts, lse_parts, n, rows, static_cast<__nv_bfloat16 *>(out), lse_out);
+          o_parts, lse_parts, n, rows, static_cast<__nv_bfloat16 *>(out), lse_out, status);
     return cudaGetLastError();
   }
   const int rows_per_block = (256 / 32) * (d == 128 ? 1 : 2);
@@ -193,10 +198,10 @@ cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int n
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   if (d == 128)
     lse_merge_kernel<128><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-        o_parts, lse_parts, n, rows, static_cast<__nv_bfloat16 *>(out), lse_out);
+        o_parts, lse_parts, n, rows, static_cast<__nv_bfloat16 *>(out), lse_out, status);
   else
     lse_merge_kernel<64><<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-        o_parts, lse_parts, n, rows, static_cast<__nv_bfloat16 *>(out), lse_out);
+        o_parts, lse_parts, n, rows, static_cast<__nv_bfloat16 *>(out), lse_out, status);
   return cudaGetLastError();
 }
 

@@ -11,6 +11,23 @@ namespace ra {
 // ----------------------------------------------------------------- status --
 // Device status codes (match RA_ERR_* in ringattn.h).
 constexpr int kStatusTimeout = -5;
+constexpr int kStatusBounds = -7;
+
+// Bounds checks of the RA_CHECKS build.  RA_IN_BOUNDS(cond, status) is true
+// when `cond` holds; when it does not, the first such failure since the last
+// ra_get_status is recorded in the status word (RA_ERR_BOUNDS) and the caller
+// skips the access (a store) or redirects it to coordinate 0 (a TMA load,
+// so that its barrier still completes).  Without RA_CHECKS the macro is the
+// constant true and the condition is never evaluated.
+__device__ __forceinline__ bool bounds_ok(bool cond, int *status) {
+  if (!cond) atomicCAS(status, 0, kStatusBounds);
+  return cond;
+}
+#ifdef RA_CHECKS
+#define RA_IN_BOUNDS(cond, status) (::ra::bounds_ok((cond), (status)))
+#else
+#define RA_IN_BOUNDS(cond, status) true
+#endif
 
 struct Watchdog {
   int *status;         // global status word (first error wins)
@@ -257,6 +274,11 @@ __device__ __forceinline__ float lg2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// The two bf16 values of a pair packed by pack_bf16x2, widened exactly.
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

@@ -64,6 +64,10 @@ struct AttnParams {
   // key tiles in the first rank's ring order.
   int rem_pack;
   WatchdogParams wd;
+  // Extents for the RA_CHECKS build's bounds checks (set by launch_ring_attn):
+  // rows of the Q and K/V row matrices, output rows per part, output parts.
+  int64_t chk_q_rows, chk_kv_rows, chk_out_rows;
+  int chk_parts;
 };
 
 // Backward pass (attn_bwd.cu).  All tensors [BH, S, d] in sharded order.
@@ -93,15 +97,21 @@ cudaError_t launch_ring_attn(const void *q, int64_t q_total_rows, const void *k,
 
 // Row permutation kernels (shard.cu).  mode: 0 shard, 1 unshard (layout, P),
 // 2 frame transpose [T,N] -> [N,T], 3 back.  row_bytes: 128, 256 (bf16 rows) or 4 (fp32).
+// status: the device status word (bounds checks of the RA_CHECKS build).
 cudaError_t launch_row_permute(const void *x, void *y, int64_t BH, int64_t S, int row_bytes,
-                               int mode, int64_t a, int64_t b, int layout, cudaStream_t stream);
+                               int mode, int64_t a, int64_t b, int layout, int *status,
+                               cudaStream_t stream);
 
 // lse_merge kernel (merge.cu).
 cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int n, int64_t rows,
-                             int d, void *out, float *lse_out, cudaStream_t stream);
+                             int d, void *out, float *lse_out, int *status, cudaStream_t stream);
 
 // Watchdog self-test kernel (attn_fwd.cu).
 cudaError_t launch_watchdog_selftest(const WatchdogParams &wd, cudaStream_t stream);
+
+// Bounds-check self-test kernel (attn_fwd.cu): checks one index against a
+// bound it exceeds, touching no memory through it.
+cudaError_t launch_checks_selftest(int *status, cudaStream_t stream);
 
 // Scratch bytes factored_attn uses for these sizes and this P (api.cu): 0
 // when every rank chunk of T / P frames fits one tile, otherwise

@@ -14,6 +14,7 @@
 // row, so both sides are fully coalesced 128-byte lines.
 #include <stdint.h>
 
+#include "ra_device.cuh"
 #include "ra_internal.h"
 
 namespace ra {
@@ -97,7 +98,7 @@ __device__ __forceinline__ uint32_t source_row(const PermuteArgs &p, uint32_t o)
 template <typename Vec, int PIECES>
 __global__ void __launch_bounds__(256) row_permute_kernel(const Vec *__restrict__ x,
                                                           Vec *__restrict__ y, int64_t total_rows,
-                                                          PermuteArgs p) {
+                                                          PermuteArgs p, int *status) {
   constexpr int kUnroll = 4;
   const int64_t total = total_rows * PIECES;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(256) row_permute_kernel(const Vec *__restrict_
           const uint32_t bh = r32 / S, o = r32 - bh * S;
           src = static_cast<int64_t>(bh * S + source_row(p, o));
         }
+        if (!RA_IN_BOUNDS(src >= 0 && src < total_rows, status)) continue;
         v[u] = x[src * PIECES + piece];
         dst[u] = e;
       }
@@ -142,25 +144,27 @@ int grid_for(int64_t work, int threads) {
 }  // namespace
 
 cudaError_t launch_row_permute(const void *x, void *y, int64_t BH, int64_t S, int row_bytes,
-                               int mode, int64_t a, int64_t b, int layout, cudaStream_t stream) {
+                               int mode, int64_t a, int64_t b, int layout, int *status,
+                               cudaStream_t stream) {
   const int64_t rows = BH * S;
   if (rows == 0) return cudaSuccess;
+  if (status == nullptr) return cudaErrorInvalidValue;
   PermuteArgs p{S, mode, a, b, layout};
   if (row_bytes % 16 == 0) {
     const int pieces = row_bytes / 16;
     const int grid = grid_for(rows * pieces / 4, 256);
     if (pieces == 16)
       row_permute_kernel<uint4, 16><<<grid, 256, 0, stream>>>(
-          static_cast<const uint4 *>(x), static_cast<uint4 *>(y), rows, p);
+          static_cast<const uint4 *>(x), static_cast<uint4 *>(y), rows, p, status);
     else if (pieces == 8)
       row_permute_kernel<uint4, 8><<<grid, 256, 0, stream>>>(
-          static_cast<const uint4 *>(x), static_cast<uint4 *>(y), rows, p);
+          static_cast<const uint4 *>(x), static_cast<uint4 *>(y), rows, p, status);
     else
       return cudaErrorInvalidValue;
   } else if (row_bytes == 4) {
     const int grid = grid_for(rows / 4, 256);
     row_permute_kernel<uint32_t, 1><<<grid, 256, 0, stream>>>(
-        static_cast<const uint32_t *>(x), static_cast<uint32_t *>(y), rows, p);
+        static_cast<const uint32_t *>(x), static_cast<uint32_t *>(y), rows, p, status);
   } else {
     return cudaErrorInvalidValue;
   }

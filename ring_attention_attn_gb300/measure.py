@@ -10,7 +10,7 @@ bandwidth for permutations and merges).  Usage:
     python -m ring_attention_attn_gb300.measure [--path NAME ...] [--reps N]
 
 Paths: shard, transpose, merge, ring_c1, ring_c2, ring_c3, rank_c5, factored_c4,
-overlap_c3, ulysses_c3, allgather_c3, reducescatter_c3, bwd_c3.
+factored_c4_unfolded, overlap_c3, ulysses_c3, allgather_c3, reducescatter_c3, bwd_c3.
 """
 from __future__ import annotations
 
@@ -114,8 +114,10 @@ def run(paths, reps):
                                                      lse=lp), max(3, reps // 4))
             emit(path, ms, acc.attention_flops(H, L, S, d), "TFLOP/s", "tensor",
                  form="per-step fp32 partials")
-        elif path == "factored_c4":
+        elif path in ("factored_c4", "factored_c4_unfolded"):
             B, H, T, N, d, P = 1, 24, 48, 900, 128, 4
+            # unfolded: the temporal ring as four 12-frame steps
+            ra.ra_set_temporal_fold(path == "factored_c4")
             q, k, v = qkv(B, H, T * N, d)
             ws = torch.empty(ra.factored_attn_workspace(B, H, T, N, d), dtype=torch.uint8,
                              device="cuda")
@@ -123,6 +125,7 @@ def run(paths, reps):
                     torch.empty_like(q), torch.empty((B, H, T * N), device="cuda"))
             ms = _time(lambda: ra.factored_attn(q, k, v, T, N, P, workspace=ws, outs=outs), reps)
             sp, tp = acc.factored_flops(B * H, T, N, d)
+            ra.ra_set_temporal_fold(True)
             emit(path, ms, sp + tp, "TFLOP/s", "tensor", spatial_flops=sp, temporal_flops=tp)
         elif path.endswith("_c3"):
             B, H, S, d, P = 1, 24, 14400, 128, 4
@@ -163,7 +166,7 @@ def run(paths, reps):
 
 
 ALL = ["shard", "transpose", "merge", "ring_c1", "ring_c2", "ring_c3", "rank_c5", "factored_c4",
-       "overlap_c3", "ulysses_c3", "allgather_c3", "reducescatter_c3", "bwd_c3"]
+       "factored_c4_unfolded", "overlap_c3", "ulysses_c3", "allgather_c3", "reducescatter_c3", "bwd_c3"]
 
 
 if __name__ == "__main__":

@@ -123,3 +123,16 @@ def test_python_binding_rejects_cpu_tensors():
     x = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         ra.ring_attn_fwd(x, x, x, 2)
+
+
+def test_checked_build_compiles_and_exports_the_same_symbols():
+    """The RA_CHECKS build (device bounds checks) builds from the same sources
+    and exports the header's symbols; it says so through ra_checks_enabled."""
+    from ring_attention_attn_gb300 import build as ra_build
+    path = ra_build.build(checks=True)
+    lib = ctypes.CDLL(path)
+    for n in _declared():
+        assert hasattr(lib, n), n
+    lib.ra_checks_enabled.restype = ctypes.c_int
+    assert lib.ra_checks_enabled() == 1
+    assert _abi.lib().ra_checks_enabled() == 0

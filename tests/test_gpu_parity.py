@@ -407,9 +407,14 @@ def test_cp_forms_c3_every_tile(form):
                                           (1, 1, 48, 5, 128, 1),   # 48-frame chunks: 2 per tile
                                           (1, 1, 260, 3, 64, 2),   # 130-frame chunks: not packed
                                           (1, 2, 130, 4, 128, 1)])
-def test_factored_small_full(B, H, T, N, d, P):
+@pytest.mark.parametrize("fold", [True, False])
+def test_factored_small_full(B, H, T, N, d, P, fold):
     q, k, v = synth.make_custom((B, H, T * N, d), (B, H, T * N, d), seed=99 + T + P)
-    os_, ls, ot, lt = ra.factored_attn(q.cuda(), k.cuda(), v.cuda(), T, N, P)
+    ra.ra_set_temporal_fold(fold)
+    try:
+        os_, ls, ot, lt = ra.factored_attn(q.cuda(), k.cuda(), v.cuda(), T, N, P)
+    finally:
+        ra.ra_set_temporal_fold(True)
     torch.cuda.synchronize()
     assert ra.ra_get_status() == 0
     ro, rl = oracle.factored(q, k, v, T, N, "spatial")
@@ -418,13 +423,19 @@ def test_factored_small_full(B, H, T, N, d, P):
     _cmp(ot, lt, ro, rl)
 
 
-def test_factored_c4_every_tile():
+@pytest.mark.parametrize("fold", [True, False])
+def test_factored_c4_every_tile(fold):
     """48 frames x 900 tokens, H = 24: spatial output on one token of every
     128-row query tile of every frame and head (9,216 rows, lanes rotating);
-    temporal output on every token (all 5,400 packed tiles per call)."""
+    temporal output on every token, with the ring's four 12-frame chunks
+    folded into two blocks (the default) and as four steps."""
     w = synth.WORKLOADS["c4"]
     q, k, v = synth.make_qkv(w)
-    os_, ls, ot, lt = ra.factored_attn(q.cuda(), k.cuda(), v.cuda(), w.T, w.N, w.P)
+    ra.ra_set_temporal_fold(fold)
+    try:
+        os_, ls, ot, lt = ra.factored_attn(q.cuda(), k.cuda(), v.cuda(), w.T, w.N, w.P)
+    finally:
+        ra.ra_set_temporal_fold(True)
     torch.cuda.synchronize()
     assert ra.ra_get_status() == 0
     rows = synth.tile_rows(w.B * w.H * w.T, w.N, w.N)
