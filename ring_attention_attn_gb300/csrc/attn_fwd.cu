@@ -75,7 +75,7 @@ struct Cfg {
   static constexpr int kOffKV = 2 * kQTile;
   static constexpr int kOffBar = kOffKV + kSlots * kKVTile;
   static constexpr int kBarBytes = 512;
-  static_assert(8 * (9 + 2 * kSlots) <= 496, "barriers overlap the TMEM slot");
+  static_assert(8 * (9 + 2 * kSlots + 2) <= 496, "barriers overlap the TMEM slot");
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
 };
 
@@ -89,6 +89,13 @@ enum : int {
   kBarQEmpty = 8,  // the Q pair's last QK^T has completed
   kBarKVFull = 9,  // +slot; kv_empty follows the kv_full block
 };
+// Split units (PK 3) use two more barriers after the K/V block: the softmax
+// warpgroups' (m, l) exchange and "both O accumulators read" (256 arrivals
+// each).
+template <int D>
+__device__ __forceinline__ int bar_xchg() { return kBarKVFull + 2 * Cfg<D>::kSlots; }
+template <int D>
+__device__ __forceinline__ int bar_ofree() { return kBarKVFull + 2 * Cfg<D>::kSlots + 1; }
 constexpr int kTmemSlotOff = 496;
 constexpr int kAbortOff = 500;
 constexpr uint32_t kTmemCols = 512;
@@ -106,12 +113,13 @@ struct Unit {
 // its units cost about half of the others; they are numbered last so that
 // the block scheduler, which hands out CTAs in index order, packs them into
 // the final, partial wave (longest units first).
-template <bool REM>
+template <bool REM, bool SPLIT>
 __device__ __forceinline__ Unit decode_unit(const AttnParams &p, int u) {
   Unit w;
   w.rem = false;
   int np = p.n_pairs, pair_base = 0;
-  if (p.n_pairs > 1 && p.L - static_cast<int64_t>(p.n_pairs - 1) * 2 * kBM <= kBM) {
+  // (Split units hold one query tile each: all cost alike, no reordering.)
+  if (!SPLIT && p.n_pairs > 1 && p.L - static_cast<int64_t>(p.n_pairs - 1) * 2 * kBM <= kBM) {
     const int heavy = (p.n_pairs - 1) * p.n_stepgroups * p.n_ranks * p.G * p.BH;
     if (u < heavy) {
       np = p.n_pairs - 1;
@@ -194,15 +202,18 @@ struct UnitGeo {
   bool has_q1;
 };
 
-template <bool CAUSAL, bool REM>
+template <bool CAUSAL, bool REM, bool SPLIT = false>
 __device__ __forceinline__ UnitGeo unit_geo(const AttnParams &p, int u) {
   UnitGeo g;
-  g.w = decode_unit<REM>(p, u);
-  g.pair_row0 = static_cast<int64_t>(g.w.pair) * 2 * kBM;
+  g.w = decode_unit<REM, SPLIT>(p, u);
+  // Split units: "pair" counts single query tiles and there is no tile 1.
+  constexpr int kRows = SPLIT ? kBM : 2 * kBM;
+  g.pair_row0 = static_cast<int64_t>(g.w.pair) * kRows;
   // Packed mode pairs rank chunks: tile 1 is the next rank's chunk.
-  g.has_q1 = p.pack ? (p.pack_ranks > 0 && g.w.rank + 1 < p.rank_begin + p.pack_ranks)
-                    : g.pair_row0 + kBM < p.L;
-  g.gq_max = CAUSAL ? zz_pos(g.w.rank, min64(g.pair_row0 + 2 * kBM - 1, p.L - 1), p.L >> 1, p.P)
+  g.has_q1 = SPLIT    ? false
+             : p.pack ? (p.pack_ranks > 0 && g.w.rank + 1 < p.rank_begin + p.pack_ranks)
+                      : g.pair_row0 + kBM < p.L;
+  g.gq_max = CAUSAL ? zz_pos(g.w.rank, min64(g.pair_row0 + kRows - 1, p.L - 1), p.L >> 1, p.P)
                       : 0;
   return g;
 }
@@ -216,7 +227,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<D>;
   // PK: 0 = row tiles, 1 = packed short problems, 2 = packed with 16 or 32
   // rows per problem (warp-packed softmax).
-  constexpr bool kPack = PK != 0;
+  // PK 3 = split units: one query tile per unit whose key tiles alternate
+  // between the two softmax warpgroups (each with its own m, l and O), merged
+  // in the epilogue; for launches with fewer units than SMs.
+  constexpr bool kPack = PK == 1 || PK == 2;
+  constexpr bool kSplit = PK == 3;
+  static_assert(!kSplit || (!OUT_F32 && !REM), "split units: bf16 output, no stacked rows");
   // REM: launches with packed remainders (rem_pack > 0), non-causal row
   // tiles only.
   static_assert(!REM || (PK == 0 && !CAUSAL), "packed remainders: non-causal row tiles");
@@ -248,6 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(kv_full0 + 8 * s, 1);
       mbar_init(kv_empty0 + 8 * s, 1);
+    }
+    if (kSplit) {
+      mbar_init(bar0 + 8 * bar_xchg<D>(), 256);
+      mbar_init(bar0 + 8 * bar_ofree<D>(), 256);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -299,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int n_loaded = 0;  // Q pairs loaded
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const UnitGeo g = unit_geo<CAUSAL, kRem>(p, u);
+        const UnitGeo g = unit_geo<CAUSAL, kRem, kSplit>(p, u);
         const Unit &w = g.w;
         TileIter ti;
         ti.init(p, w);
@@ -350,11 +370,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 (!g.has_q1 || static_cast<int64_t>(qy) + kBM < p.chk_q_rows),
                             wd.status))
             qy = 0;
-          mbar_arrive_expect_tx(qfull, 2 * C::kQTile);
+          // Split units read one query tile (the Q1 buffer holds the
+          // warpgroups' (m, l) exchange instead).
+          mbar_arrive_expect_tx(qfull, kSplit ? C::kQTile : 2 * C::kQTile);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c) {
             tma_load_2d(sbase + C::kOffQ0 + c * C::kChunkBytes, &tm_q, c * 64, qy, qfull);
-            tma_load_2d(sbase + C::kOffQ1 + c * C::kChunkBytes, &tm_q, c * 64, qy + kBM, qfull);
+            if (!kSplit)
+              tma_load_2d(sbase + C::kOffQ1 + c * C::kChunkBytes, &tm_q, c * 64, qy + kBM,
+                          qfull);
           }
         }
         ++n_loaded;
@@ -424,8 +448,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       int n_loaded = 0;    // Q pairs consumed
       int jt[2] = {0, 0};  // tiles handed to each softmax warpgroup so far
       bool ok = true;
+      if constexpr (kSplit) {
+        // Split units: visible key tile t of the unit goes to warpgroup t % 2;
+        // both S_i read the one query tile.  S of tile t + 2 is issued right
+        // after PV of tile t (it overwrites the same TMEM columns).
+        int n_units_done = 0;  // units with at least one tile (O_done / O_free phases)
+        for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+          const UnitGeo g = unit_geo<CAUSAL, kRem, kSplit>(p, u);
+          const Unit &w = g.w;
+          TileIter ts;  // next tile whose S is to be issued
+          ts.init(p, w);
+          ts.settle<CAUSAL>(p, w, n_t, g.gq_max);
+          if (!ts.valid(w)) continue;
+          if (!(ok = mbar_wait(bar0 + 8 * kBarQFull, n_loaded & 1, wd, abort_flag))) break;
+          ++n_loaded;
+          tc_fence_after();
+          const int base = it;
+          int ns = 0;  // tiles whose S has been issued
+          auto issue_next_s = [&](int i) -> bool {
+            const int seq = base + 2 * ns;
+            if (!mbar_wait(kv_full0 + 8 * (seq % C::kSlots), (seq / C::kSlots) & 1, wd,
+                           abort_flag))
+              return false;
+            tc_fence_after();
+            issue_qk<D>(tmem + col_s(i), dq[0],
+                        dk0 + static_cast<uint64_t>((seq % C::kSlots) * (C::kKVTile >> 4)),
+                        idesc_s);
+            mma_commit_e(bar0 + 8 * (kBarSFull + i));
+            mma_commit_e(kv_empty0 + 8 * (seq % C::kSlots));
+            ++ns;
+            ++ts.t;
+            ts.settle<CAUSAL>(p, w, n_t, g.gq_max);
+            // The unit's last QK^T has been issued: the Q buffer is free once
+            // it completes.
+            if (!ts.valid(w)) mma_commit_e(bar0 + 8 * kBarQEmpty);
+            return true;
+          };
+          ok = issue_next_s(0) && (!ts.valid(w) || issue_next_s(1));
+          issued = true;
+          for (int t = 0; ok && t < ns; ++t) {
+            const int i = t & 1;
+            const int seq_v = base + 2 * t + 1;
+            if (!(ok = mbar_wait(kv_full0 + 8 * (seq_v % C::kSlots), (seq_v / C::kSlots) & 1, wd,
+                                 abort_flag)))
+              break;
+            if (!(ok = mbar_wait(bar0 + 8 * (kBarPFull + i), (jt[i] + (t >> 1)) & 1, wd,
+                                 abort_flag)))
+              break;
+            // The first PV of a unit overwrites O_i: both warpgroups must
+            // have read the previous unit's accumulators.
+            if (t < 2 && n_units_done > 0 &&
+                !(ok = mbar_wait(bar0 + 8 * bar_ofree<D>(), (n_units_done - 1) & 1, wd,
+                                 abort_flag)))
+              break;
+            tc_fence_after();
+            issue_o(i, seq_v % C::kSlots, t >= 2);
+            mma_commit_e(kv_empty0 + 8 * (seq_v % C::kSlots));
+            if (ts.valid(w) && !(ok = issue_next_s(i))) break;
+          }
+          if (!ok) break;
+          it = base + 2 * ns;
+          for (int i = 0; i < 2; ++i) mma_commit_e(bar0 + 8 * (kBarODone + i));
+          jt[0] += (ns + 1) >> 1;
+          jt[1] += ns >> 1;
+          ++n_units_done;
+        }
+      } else
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const UnitGeo g = unit_geo<CAUSAL, kRem>(p, u);
+        const UnitGeo g = unit_geo<CAUSAL, kRem, kSplit>(p, u);
         const Unit &w = g.w;
         const bool has_q1 = g.has_q1;
         const int nq = has_q1 ? 2 : 1;
@@ -522,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n_done = 0;  // units whose O this warpgroup has read (O_done phases)
     // The next unit's geometry is decoded while the last PV of the current
     // one runs, off the path from this unit's epilogue to the next S.
-    UnitGeo g_next = unit_geo<CAUSAL, kRem>(p, blockIdx.x);
+    UnitGeo g_next = unit_geo<CAUSAL, kRem, kSplit>(p, blockIdx.x);
     // Packed tiles: this thread's row is frame row_fr of problem row_pr in
     // every unit.
     const int row_pr = kPack ? row / p.pLrow : 0;
@@ -531,13 +621,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const UnitGeo g = g_next;
       const int u_next = u + static_cast<int>(gridDim.x);
       const Unit &w = g.w;
-      if (!(wg == 0 || g.has_q1)) {
-        if (u_next < n_units) g_next = unit_geo<CAUSAL, kRem>(p, u_next);
+      if (!kSplit && !(wg == 0 || g.has_q1)) {
+        if (u_next < n_units) g_next = unit_geo<CAUSAL, kRem, kSplit>(p, u_next);
         continue;
       }
       // Row within the rank's chunk; in packed mode within the tile, whose
-      // rank is w.rank + wg.
-      const int64_t qi = kPack ? row : g.pair_row0 + wg * kBM + row;
+      // rank is w.rank + wg; split units: both warpgroups hold the same rows.
+      const int64_t qi = kPack ? row : g.pair_row0 + (kSplit ? 0 : wg * kBM) + row;
       // Packed mode: row qi is frame qi % pLrow of the chunk of problem
       // g * pack + qi / pLrow (pLrow >= Lf rows per problem; rows past Lf
       // hold the next frames and are not written) and sees only the first Lf
@@ -564,10 +654,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // dominant probability (up to 2^-9 relative) straight into O.
       float m_ref = -INFINITY, l = 0.f, lr = 0.f;
       int j = 0;
+      int tv = 0;  // visible tiles of the unit walked (split units take every other)
       TileIter ti;
       ti.init(p, w);
       ti.settle<CAUSAL>(p, w, n_t, g.gq_max);
       while (ti.valid(w)) {
+        if (kSplit && (tv & 1) != wg) {
+          ++tv;
+          ++ti.t;
+          ti.settle<CAUSAL>(p, w, n_t, g.gq_max);
+          continue;
+        }
         const bool ok = __all_sync(
             0xffffffffu, mbar_wait(bar0 + 8 * (kBarSFull + wg), (jt + j) & 1, wd, abort_flag));
         if (!ok) break;
@@ -724,13 +821,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(bar0 + 8 * (kBarPFull + wg));
         ++j;
+        ++tv;
         ++ti.t;
         ti.settle<CAUSAL>(p, w, n_t, g.gq_max);
       }
       __syncwarp();
       const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
       if (aborted) break;
-      if (u_next < n_units) g_next = unit_geo<CAUSAL, kRem>(p, u_next);
+      if (u_next < n_units) g_next = unit_geo<CAUSAL, kRem, kSplit>(p, u_next);
+      if constexpr (kSplit) {
+        // Merge the two warpgroups' partial softmax states of each row:
+        //   M = max(m0, m1),  a_i = 2^(m_i - M),  l = a0 l0 + a1 l1,
+        //   O = (a0 O0 + a1 O1) / l,  LSE = (M + log2 l) ln 2,
+        // the (m, l) pairs exchanged through shared memory (double-buffered
+        // by unit), O0 and O1 read from tensor memory; warpgroup i writes
+        // columns [i D/2, (i+1) D/2) of the row.
+        jt += j;
+        if (tv == 0) continue;  // no visible key tile: the MMA warp skipped the unit too
+        float *xb = reinterpret_cast<float *>(smem + C::kOffQ1) + (n_done & 1) * (4 * kBM);
+        xb[(wg * kBM + row) * 2] = m_ref;
+        xb[(wg * kBM + row) * 2 + 1] = l;
+        mbar_arrive(bar0 + 8 * bar_xchg<D>());
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(bar0 + 8 * bar_xchg<D>(), n_done & 1, wd, abort_flag)))
+          break;
+        const float m_o = xb[((1 - wg) * kBM + row) * 2];
+        const float l_o = xb[((1 - wg) * kBM + row) * 2 + 1];
+        const float M = fmaxf(m_ref, m_o);
+        const float a_s = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - M);
+        const float a_o = (m_o == -INFINITY) ? 0.f : ex2(m_o - M);
+        const float lt = a_s * l + a_o * l_o;
+        const float inv = (lt > 0.f) ? 1.f / lt : 0.f;
+        const float c0 = (wg == 0 ? a_s : a_o) * inv, c1 = (wg == 0 ? a_o : a_s) * inv;
+        const bool have1 = tv >= 2;  // warpgroup 1 met a tile: O1 holds this unit's sum
+        const bool done = __all_sync(
+            0xffffffffu, mbar_wait(bar0 + 8 * kBarODone, n_done & 1, wd, abort_flag) &&
+                             mbar_wait(bar0 + 8 * (kBarODone + 1), n_done & 1, wd, abort_flag));
+        ++n_done;
+        if (!done) break;
+        tc_fence_after();
+        const int64_t orow = w.q_row0 + qi;
+        if (row_valid && !RA_IN_BOUNDS(orow >= 0 && orow < p.chk_out_rows, wd.status))
+          row_valid = false;
+        __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * D;
+        const uint32_t tO0 = tmem + lane_bits + col_o(0), tO1 = tmem + lane_bits + col_o(1);
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+          const int c = wg * (D / 64) + cc;
+          float o0[32], o1[32];
+          tmem_ld32(tO0 + c * 32, o0);
+          if (have1) tmem_ld32(tO1 + c * 32, o1);
+          tmem_wait_ld();
+          if (!have1) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o1[x] = 0.f;
+          }
+          if (row_valid) {
+            uint4 *dst = reinterpret_cast<uint4 *>(out + c * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              uint32_t v4[4];
+#pragma unroll
+              for (int y = 0; y < 4; ++y) {
+                const int e = 8 * x + 2 * y;
+                v4[y] = pack_bf16x2(fmaf(c0, o0[e], c1 * o1[e]),
+                                    fmaf(c0, o0[e + 1], c1 * o1[e + 1]));
+              }
+              dst[x] = make_uint4(v4[0], v4[1], v4[2], v4[3]);
+            }
+          }
+        }
+        // Both accumulators have been read: the next unit's PVs may start.
+        tc_fence_before();
+        mbar_arrive(bar0 + 8 * bar_ofree<D>());
+        if (row_valid && wg == 0) p.lse[orow] = (lt > 0.f) ? (M + lg2(lt)) * kLn2 : -INFINITY;
+        continue;
+      }
       bool have_o = false;
       if (j > 0) {
         have_o = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (kBarODone + wg), n_done & 1, wd,
@@ -935,6 +1101,16 @@ cudaError_t launch_kernel(const CUtensorMap &mq, const CUtensorMap &mk, const CU
   return cudaGetLastError();
 }
 
+// Multiprocessors of device `dev` (cached; 0 on failure).
+int sm_count(int dev) {
+  static int sms[64] = {};
+  if (dev < 0 || dev >= 64) return 0;
+  if (sms[dev] == 0 &&
+      cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms[dev] = 0;
+  return sms[dev];
+}
+
 template <int D, bool OUT_F32, int PK, bool CAUSAL>
 cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                            const CUtensorMap &mqr, const AttnParams &p, int64_t n_units,
@@ -948,14 +1124,23 @@ cudaError_t launch_variant(const CUtensorMap &mq, const CUtensorMap &mk, const C
   // + gridDim.x, ..., so that a CTA's next query pair and key tiles load
   // while its current pair finishes.  Long units get one CTA each and the
   // block scheduler balances them (static striding costs ~1% there).
-  static int sms[64] = {};
-  if (sms[dev] == 0) {
-    e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-  }
+  const int sms = sm_count(dev);
+  if (sms <= 0) return cudaErrorInvalidDevice;
   const int64_t tiles_per_unit = ((p.L + kBN - 1) / kBN) * p.steps_per_group;
   const int64_t grid =
-      (tiles_per_unit <= kPersistMaxTiles && n_units > sms[dev]) ? sms[dev] : n_units;
+      (tiles_per_unit <= kPersistMaxTiles && n_units > sms) ? sms : n_units;
+  if constexpr (PK == 0 && !OUT_F32) {
+    // A launch of fewer pair units than SMs runs as split units (one query
+    // tile each, its key tiles shared by the two softmax warpgroups): twice
+    // the units, half the work on the longest one.  One unit per CTA.
+    if (p.rem_pack == 0 && n_units < sms) {
+      AttnParams ps = p;
+      ps.n_pairs = static_cast<int>((p.L + kBM - 1) / kBM);
+      const int64_t nu = static_cast<int64_t>(ps.BH) * ps.G * ps.n_stepgroups * ps.n_ranks *
+                         ps.n_pairs;
+      return launch_kernel<D, false, 3, CAUSAL, false>(mq, mk, mv, mqr, ps, nu, nu, dev, stream);
+    }
+  }
   if constexpr (PK == 0 && !CAUSAL) {
     if (p.rem_pack > 0)
       return launch_kernel<D, OUT_F32, PK, CAUSAL, true>(mq, mk, mv, mqr, p, n_units, grid, dev,

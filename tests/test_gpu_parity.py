@@ -129,6 +129,13 @@ CASES = [
     (1, 3, 888, 128, 3, False),   # 296-row chunks: 3 x 40 rows
     (2, 1, 2112, 64, 8, False),   # 264-row chunks: 8 x 8 rows
     (1, 1, 656, 128, 2, False),   # 328-row chunks: 2 x 72 rows do not fit
+    # at least as many query-tile pairs as SMs: pair units (fewer run as split
+    # units, one query tile each, key tiles alternating between warpgroups)
+    (1, 40, 2048, 64, 2, True),
+    (1, 24, 2048, 128, 4, True),
+    (1, 40, 2048, 128, 2, False),
+    (1, 3, 384, 64, 1, False),    # split units of 3 key tiles: odd count per warpgroup
+    (1, 2, 128, 128, 1, True),    # one key tile: the second warpgroup meets none
 ]
 
 
