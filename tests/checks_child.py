@@ -50,7 +50,7 @@ def main():
         ro, rl = oracle.attention(q, k, v, causal=w.causal)
         _close(o, l, ro, rl)
     # stacked last rows, per-step partials + merge, overlap, CP forms
-    B, H, S, d, P = 1, 2, 1088, 128, 4
+    B, H, S, d, P = 1, 4, 1088, 128, 4  # Ulysses needs H % P == 0
     q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=5)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     ro, rl = oracle.attention(q, k, v)
