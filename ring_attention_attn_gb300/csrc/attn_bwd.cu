@@ -421,26 +421,35 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUten
       // Keys [0, nvis) of the tile are visible; when every row of the warp
       // sees all of this half, no column needs a mask.
       const bool full = __all_sync(0xffffffffu, nvis >= 64 * h + 64);
+      // Four 16-column chunks, software-pipelined: chunk c + 1's TMEM loads
+      // are in flight while chunk c is computed (two chunks of S and dP live).
+      float sv[2][16], pv[2][16];
+      tmem_ld16(tS, sv[0]);
+      tmem_ld16(tP, pv[0]);
+      tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float sv[32], pv[32];
-        tmem_ld32(tS + c * 32, sv);
-        tmem_ld32(tP + c * 32, pv);
-        tmem_wait_ld();
-        uint32_t pk[16];
+      for (int c = 0; c < 4; ++c) {
+        const int b = c & 1;
+        if (c < 3) {
+          tmem_ld16(tS + (c + 1) * 16, sv[b ^ 1]);
+          tmem_ld16(tP + (c + 1) * 16, pv[b ^ 1]);
+        }
+        uint32_t pk[8];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const float2 a = ffma2(make_float2(sv[2 * x], sv[2 * x + 1]), sl2v, nlse2);
+        for (int x = 0; x < 8; ++x) {
+          const float2 a = ffma2(make_float2(sv[b][2 * x], sv[b][2 * x + 1]), sl2v, nlse2);
           float2 e = make_float2(ex2(a.x), ex2(a.y));
           if (!full) {
-            const int cc = 64 * h + c * 32 + 2 * x;
+            const int cc = 64 * h + c * 16 + 2 * x;
             e.x = cc < nvis ? e.x : 0.f;
             e.y = cc + 1 < nvis ? e.y : 0.f;
           }
-          const float2 ds = fmul2(e, fadd2(make_float2(pv[2 * x], pv[2 * x + 1]), nD2));
+          const float2 ds = fmul2(e, fadd2(make_float2(pv[b][2 * x], pv[b][2 * x + 1]), nD2));
           pk[x] = pack_bf16x2(ds.x, ds.y);
         }
-        tmem_st16(tS + c * 16, pk);
+        // dS of columns [16c, 16c + 16) over S columns [8c, 8c + 8): already read.
+        tmem_st8(tS + c * 8, pk);
+        if (c < 3) tmem_wait_ld();
       }
       tmem_wait_st();
       tc_fence_before();
@@ -700,49 +709,65 @@ __device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUte
       ld[row < 64 ? qi : 64 + qi] = val;
       val = tn.valid() ? staged(tn) : 0.f;         // next tile's value, in flight
       mbar_arrive(bb.b(kBLd + 2 * h + (j & 1)));  // release: the value above
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(bb.b(kBLd + 2 * h + (j & 1)), (j >> 1) & 1, wd, abort_flag)))
-        break;
       // Visible queries of this key: positions >= its own (a suffix of the tile).
       int first = 0, last = static_cast<int>(nq);
       if (!kvalid) first = last;
       else if (CAUSAL) first = causal_visible(ti.blk, q0, gk - 1, p.L, p.P);
       if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBH + h), j & 1, wd, abort_flag))) break;
       tc_fence_after();
+      // Every thread's staged value is in shared memory (waited after S^T, so
+      // the barrier's round trip overlaps the wait for the tensor core).  A
+      // buffer cannot run a phase ahead of this wait: the next arrival on it
+      // (two tiles on) follows this tile's S^T wait on every thread, which
+      // needs all of this tile's computed-half arrivals.
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(bb.b(kBLd + 2 * h + (j & 1)), (j >> 1) & 1, wd, abort_flag)))
+        break;
       // When every key row of the warp sees every query of this half, no
       // column needs a mask.
       const bool full = __all_sync(0xffffffffu, first <= 64 * h && last >= 64 * h + 64);
       const float2 sl2v = make_float2(sl2, sl2);
+      // Four 16-column chunks, software-pipelined: chunk c + 1's TMEM loads
+      // are in flight while chunk c is computed (two chunks of S^T and dP^T
+      // live).
+      float sv[2][16], pv[2][16];
+      tmem_ld16(tS, sv[0]);
+      tmem_ld16(tP, pv[0]);
+      tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float sv[32], pv[32];
-        tmem_ld32(tS + c * 32, sv);
-        tmem_ld32(tP + c * 32, pv);
-        tmem_wait_ld();
-        uint32_t pkp[16], pks[16];
+      for (int c = 0; c < 4; ++c) {
+        const int b = c & 1;
+        if (c < 3) {
+          tmem_ld16(tS + (c + 1) * 16, sv[b ^ 1]);
+          tmem_ld16(tP + (c + 1) * 16, pv[b ^ 1]);
+        }
+        uint32_t pkp[8], pks[8];
 #pragma unroll
-        for (int y = 0; y < 8; ++y) {
-          const float4 nl = *reinterpret_cast<const float4 *>(ld + c * 32 + 4 * y);
-          const float4 nd = *reinterpret_cast<const float4 *>(ld + 64 + c * 32 + 4 * y);
+        for (int y = 0; y < 4; ++y) {
+          const float4 nl = *reinterpret_cast<const float4 *>(ld + c * 16 + 4 * y);
+          const float4 nd = *reinterpret_cast<const float4 *>(ld + 64 + c * 16 + 4 * y);
 #pragma unroll
           for (int z = 0; z < 2; ++z) {
             const int x = 2 * y + z;
-            const float2 a = ffma2(make_float2(sv[2 * x], sv[2 * x + 1]), sl2v,
+            const float2 a = ffma2(make_float2(sv[b][2 * x], sv[b][2 * x + 1]), sl2v,
                                    z ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y));
             float2 e = make_float2(ex2(a.x), ex2(a.y));
             if (!full) {
-              const int cc = 64 * h + c * 32 + 2 * x;  // column within the tile
+              const int cc = 64 * h + c * 16 + 2 * x;  // column within the tile
               e.x = cc >= first && cc < last ? e.x : 0.f;
               e.y = cc + 1 >= first && cc + 1 < last ? e.y : 0.f;
             }
-            const float2 ds = fmul2(e, fadd2(make_float2(pv[2 * x], pv[2 * x + 1]),
+            const float2 ds = fmul2(e, fadd2(make_float2(pv[b][2 * x], pv[b][2 * x + 1]),
                                              z ? make_float2(nd.z, nd.w) : make_float2(nd.x, nd.y)));
             pkp[x] = pack_bf16x2(e.x, e.y);
             pks[x] = pack_bf16x2(ds.x, ds.y);
           }
         }
-        tmem_st16(tS + c * 16, pkp);
-        tmem_st16(tP + c * 16, pks);
+        // P^T and dS^T of columns [16c, 16c + 16) over columns [8c, 8c + 8)
+        // of S^T and dP^T: already read.
+        tmem_st8(tS + c * 8, pkp);
+        tmem_st8(tP + c * 8, pks);
+        if (c < 3) tmem_wait_ld();
       }
       tmem_wait_st();
       tc_fence_before();
