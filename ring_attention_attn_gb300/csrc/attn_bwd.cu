@@ -709,20 +709,15 @@ __device__ __forceinline__ void bwd_dkv_body(const CUtensorMap &tm_q, const CUte
       ld[row < 64 ? qi : 64 + qi] = val;
       val = tn.valid() ? staged(tn) : 0.f;         // next tile's value, in flight
       mbar_arrive(bb.b(kBLd + 2 * h + (j & 1)));  // release: the value above
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(bb.b(kBLd + 2 * h + (j & 1)), (j >> 1) & 1, wd, abort_flag)))
+        break;
       // Visible queries of this key: positions >= its own (a suffix of the tile).
       int first = 0, last = static_cast<int>(nq);
       if (!kvalid) first = last;
       else if (CAUSAL) first = causal_visible(ti.blk, q0, gk - 1, p.L, p.P);
       if (!__all_sync(0xffffffffu, mbar_wait(bb.b(kBH + h), j & 1, wd, abort_flag))) break;
       tc_fence_after();
-      // Every thread's staged value is in shared memory (waited after S^T, so
-      // the barrier's round trip overlaps the wait for the tensor core).  A
-      // buffer cannot run a phase ahead of this wait: the next arrival on it
-      // (two tiles on) follows this tile's S^T wait on every thread, which
-      // needs all of this tile's computed-half arrivals.
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(bb.b(kBLd + 2 * h + (j & 1)), (j >> 1) & 1, wd, abort_flag)))
-        break;
       // When every key row of the warp sees every query of this half, no
       // column needs a mask.
       const bool full = __all_sync(0xffffffffu, first <= 64 * h && last >= 64 * h + 64);
