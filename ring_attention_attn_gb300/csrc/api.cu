@@ -129,7 +129,9 @@ int ra_cp_shard(const void *x, void *y, int64_t BH, int64_t S, int d, int P, int
   if (!x || !y) return RA_ERR_ARG;
   if (!aligned16(x) || !aligned16(y)) return RA_ERR_ALIGN;
   if (BH * S > kMaxRows) return RA_ERR_SHAPE;
-  cudaError_t e = ra::launch_row_permute(x, y, BH, S, d * 2, inverse ? 1 : 0, P, 0, layout, status_ptr(),
+  int *sw = status_ptr();
+  if (sw == nullptr) return fail_cuda(cudaGetLastError());
+  cudaError_t e = ra::launch_row_permute(x, y, BH, S, d * 2, inverse ? 1 : 0, P, 0, layout, sw,
                                          as_stream(stream));
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
@@ -142,7 +144,9 @@ int ra_frame_transpose(const void *x, void *y, int64_t BH, int64_t T, int64_t N,
   if (!x || !y) return RA_ERR_ARG;
   if (!aligned16(x) || !aligned16(y)) return RA_ERR_ALIGN;
   if (BH * T * N > kMaxRows) return RA_ERR_SHAPE;
-  cudaError_t e = ra::launch_row_permute(x, y, BH, T * N, d * 2, inverse ? 3 : 2, T, N, 0, status_ptr(),
+  int *sw = status_ptr();
+  if (sw == nullptr) return fail_cuda(cudaGetLastError());
+  cudaError_t e = ra::launch_row_permute(x, y, BH, T * N, d * 2, inverse ? 3 : 2, T, N, 0, sw,
                                          as_stream(stream));
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
@@ -349,7 +353,7 @@ int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out
     if (e == cudaSuccess && s >= 1) e = cudaEventRecord(consumed[s & 1], cs);
   }
   if (e == cudaSuccess)
-    e = ra::launch_lse_merge(o_parts, l_parts, P, BH * S, d, out, lse, status_ptr(), cs);
+    e = ra::launch_lse_merge(o_parts, l_parts, P, BH * S, d, out, lse, wd.status, cs);
   for (int i = 0; i < 2; ++i) {
     cudaEventDestroy(copied[i]);
     cudaEventDestroy(consumed[i]);
@@ -367,7 +371,9 @@ int ra_ulysses_a2a(const void *x, void *y, int B, int H, int64_t S, int d, int P
   if (!x || !y) return RA_ERR_ARG;
   if (!aligned16(x) || !aligned16(y)) return RA_ERR_ALIGN;
   if (BH * S > kMaxRows) return RA_ERR_SHAPE;
-  cudaError_t e = ra::launch_row_permute(x, y, BH, S, d * 2, inverse ? 5 : 4, P, H, B, status_ptr(),
+  int *sw = status_ptr();
+  if (sw == nullptr) return fail_cuda(cudaGetLastError());
+  cudaError_t e = ra::launch_row_permute(x, y, BH, S, d * 2, inverse ? 5 : 4, P, H, B, sw,
                                          as_stream(stream));
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
@@ -403,7 +409,7 @@ int ulysses_attn_fwd(const void *q, const void *k, const void *v, void *out, flo
   void *dst[3] = {qh, kh, vh};
   cudaError_t e;
   for (int i = 0; i < 3; ++i) {
-    e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 4, P, H, B, status_ptr(), st);
+    e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 4, P, H, B, wd.status, st);
     if (e != cudaSuccess) return fail_cuda(e);
   }
   // Head-split: B*H heads of S tokens in global order; no ring (P = 1).
@@ -425,9 +431,9 @@ int ulysses_attn_fwd(const void *q, const void *k, const void *v, void *out, flo
   p.wd = wd;
   e = ra::launch_ring_attn(qh, BH * S, kh, vh, BH * S, d, false, p, st);
   if (e != cudaSuccess) return fail_cuda(e);
-  e = ra::launch_row_permute(oh, out, BH, S, d * 2, 5, P, H, B, status_ptr(), st);
+  e = ra::launch_row_permute(oh, out, BH, S, d * 2, 5, P, H, B, wd.status, st);
   if (e != cudaSuccess) return fail_cuda(e);
-  e = ra::launch_row_permute(lh, lse, BH, S, 4, 5, P, H, B, status_ptr(), st);
+  e = ra::launch_row_permute(lh, lse, BH, S, 4, 5, P, H, B, wd.status, st);
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
 
@@ -471,8 +477,8 @@ int cp_allgather_attn_fwd(const void *q, const void *k, const void *v, void *out
   const size_t tb = ovl_part(static_cast<size_t>(BH * S) * d * 2);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   void *kg = ws + tb, *vg = ws + 2 * tb;
-  cudaError_t e = ra::launch_row_permute(k, kg, BH, S, d * 2, 6, P, H, B, status_ptr(), st);
-  if (e == cudaSuccess) e = ra::launch_row_permute(v, vg, BH, S, d * 2, 6, P, H, B, status_ptr(), st);
+  cudaError_t e = ra::launch_row_permute(k, kg, BH, S, d * 2, 6, P, H, B, wd.status, st);
+  if (e == cudaSuccess) e = ra::launch_row_permute(v, vg, BH, S, d * 2, 6, P, H, B, wd.status, st);
   if (e == cudaSuccess) {
     // Every rank's own queries (buffer r) against every block of the gathered
     // K/V, all ranks in one launch.
@@ -521,7 +527,7 @@ int cp_reducescatter_attn_fwd(const void *q, const void *k, const void *v, void 
   void *dst[3] = {qg, kg, vg};
   cudaError_t e = cudaSuccess;
   for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-    e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 6, P, H, B, status_ptr(), st);
+    e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 6, P, H, B, wd.status, st);
   if (e == cudaSuccess) {
     // Every (rank, block) pair once; the partial is filed under the block.
     ra::AttnParams p{};
@@ -548,9 +554,11 @@ int cp_reducescatter_attn_fwd(const void *q, const void *k, const void *v, void 
     p.wd = wd;
     e = ra::launch_ring_attn(qg, BH * S, kg, vg, BH * S, d, true, p, st);
   }
-  if (e == cudaSuccess) e = ra::launch_lse_merge(o_parts, l_parts, P, BH * S, d, og, lg, status_ptr(), st);
-  if (e == cudaSuccess) e = ra::launch_row_permute(og, out, BH, S, d * 2, 7, P, H, B, status_ptr(), st);
-  if (e == cudaSuccess) e = ra::launch_row_permute(lg, lse, BH, S, 4, 7, P, H, B, status_ptr(), st);
+  if (e == cudaSuccess)
+    e = ra::launch_lse_merge(o_parts, l_parts, P, BH * S, d, og, lg, wd.status, st);
+  if (e == cudaSuccess)
+    e = ra::launch_row_permute(og, out, BH, S, d * 2, 7, P, H, B, wd.status, st);
+  if (e == cudaSuccess) e = ra::launch_row_permute(lg, lse, BH, S, 4, 7, P, H, B, wd.status, st);
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
 
@@ -601,7 +609,9 @@ int lse_merge(const float *o_parts, const float *lse_parts, int n, int64_t rows,
   if (!o_parts || !lse_parts || !out || !lse_out) return RA_ERR_ARG;
   if (!aligned16(o_parts) || !aligned16(out) || !aligned16(lse_parts) || !aligned16(lse_out))
     return RA_ERR_ALIGN;
-  cudaError_t e = ra::launch_lse_merge(o_parts, lse_parts, n, rows, d, out, lse_out, status_ptr(),
+  int *sw = status_ptr();
+  if (sw == nullptr) return fail_cuda(cudaGetLastError());
+  cudaError_t e = ra::launch_lse_merge(o_parts, lse_parts, n, rows, d, out, lse_out, sw,
                                        as_stream(stream));
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
@@ -683,7 +693,7 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
     void *dst[3] = {ws + tbytes, ws + 2 * tbytes, ws + 3 * tbytes};
     const void *src[3] = {q, k, v};
     for (int i = 0; i < 3; ++i) {
-      e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 2, T, N, 0, status_ptr(), st);
+      e = ra::launch_row_permute(src[i], dst[i], BH, S, d * 2, 2, T, N, 0, wd.status, st);
       if (e != cudaSuccess) return fail_cuda(e);
     }
     tq = dst[0];
@@ -747,9 +757,9 @@ int factored_attn(const void *q, const void *k, const void *v, void *out_s, floa
     if (e != cudaSuccess) return fail_cuda(e);
   }
   if (!packed) {
-    e = ra::launch_row_permute(oT, out_t, BH, S, d * 2, 3, T, N, 0, status_ptr(), st);
+    e = ra::launch_row_permute(oT, out_t, BH, S, d * 2, 3, T, N, 0, wd.status, st);
     if (e != cudaSuccess) return fail_cuda(e);
-    e = ra::launch_row_permute(lT, lse_t, BH, S, 4, 3, T, N, 0, status_ptr(), st);
+    e = ra::launch_row_permute(lT, lse_t, BH, S, 4, 3, T, N, 0, wd.status, st);
     if (e != cudaSuccess) return fail_cuda(e);
   }
   return RA_OK;
