@@ -354,9 +354,12 @@ def run_ours(a, rank, world, local):
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    e2e_clocks = ClockSampler(local)
     if e2e_steps:
+        e2e_clocks.start()
         e2e_run(e2e_steps, e0, e1)
     torch.cuda.synchronize()
+    e2e_clock_info = e2e_clocks.stop() if e2e_steps else None
     e2e_ms = e0.elapsed_time(e1) if e2e_steps else float("nan")
     if e2e_steps:
         e2e_ms = reduce_max_ms(e2e_ms, dist, dev)
@@ -398,7 +401,8 @@ def run_ours(a, rank, world, local):
             "clocks": clock_info,
             "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "ms_per_step": (e2e_ms / e2e_steps) if e2e_steps else None},
+                    "ms_per_step": (e2e_ms / e2e_steps) if e2e_steps else None,
+                    "clocks": e2e_clock_info},
             "gpu_launches": 2 * a.steps,
         }
         if cpu is not None:
