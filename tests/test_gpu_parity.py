@@ -156,13 +156,14 @@ def _c3_rows(w):
     return np.unique(np.concatenate([rows, edge]))
 
 
-def test_ring_c3_every_tile():
+def test_ring_c3_every_row():
+    """The 14,400-token workload through the ring, every output row (345,600
+    rows, 2.5 TFLOP of fp64: about a minute on 16 host cores)."""
     w = synth.WORKLOADS["c3"]
     q, k, v = synth.make_qkv(w)
     o, l = _run_ring(q, k, v, w.P, w.causal)
-    rows = _c3_rows(w)
-    ro, rl = oracle.attention(q, k, v, rows=rows)
-    _cmp(o.reshape(-1, w.d)[rows], l.reshape(-1)[rows], ro, rl)
+    ro, rl = oracle.attention(q, k, v)
+    _cmp(o, l, ro, rl)
 
 
 @pytest.mark.parametrize("causal", [False, True])
