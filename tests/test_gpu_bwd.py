@@ -35,6 +35,9 @@ CASES = [
     (1, 1, 16, 64, 8, True),
     (1, 2, 1088, 128, 4, False),  # 272-row chunks: the ranks' last 16 rows stacked
     (1, 1, 504, 64, 3, False),    # 168-row chunks: 3 x 40 rows stacked
+    # a longer ring: 1,040-row chunks (9 tiles each, the last 16 rows of every
+    # chunk stacked), 16 heads so the oracle (parallel over heads) uses 16 cores
+    (1, 16, 4160, 128, 4, False),
 ]
 
 
