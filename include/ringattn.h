@@ -258,13 +258,15 @@ size_t factored_attn_workspace(int B, int H, int T, int N, int d);
  *    return RA_ERR_WORKSPACE and launch nothing.  Other argument errors are
  *    those of factored_attn.
  *  - The array lives in every GPU that loads the library until the process
- *    exits.  The first call on a device looks up the array's device address
- *    (once per device, with that device current); make that first call before
- *    any stream capture.  The CUDA runtime loads device code lazily by
- *    default, so that first call is also when the 64 MiB array is placed in
- *    the device's memory: it can fail there with RA_ERR_CUDA (out of memory)
- *    if the caller's own pool has already taken all device memory.  Make the
- *    first call (any sizes) before creating such a pool.
+ *    exits.  The first call on a device whose sizes need scratch (rank chunks
+ *    over 128 frames) looks up the array's device address (once per device,
+ *    with that device current); make that call before any stream capture.
+ *    The CUDA runtime loads device code lazily by default, so that call is
+ *    also when the 64 MiB array is placed in the device's memory: it can fail
+ *    there with RA_ERR_CUDA (out of memory) if the caller's own pool has
+ *    already taken all device memory, so make it before creating such a pool.
+ *    Calls whose sizes need no scratch never look the array up, and under lazy
+ *    loading never cause it to be placed in device memory.
  *  - The looked-up address is kept for the life of the process: after
  *    cudaDeviceReset, or after the primary context is destroyed and made
  *    again, this entry point must not be called on that device.

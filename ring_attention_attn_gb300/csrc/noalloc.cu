@@ -61,10 +61,15 @@ extern "C" int factored_attn_static(const void *q, const void *k, const void *v,
   // the argument error itself.)
   const size_t need = ra::factored_scratch_bytes(B, H, T, N, d, P);
   if (need > RA_STATIC_SCRATCH_BYTES) return RA_ERR_WORKSPACE;
-  void *ws = scratch_on_current_device();
-  if (ws == nullptr) return RA_ERR_CUDA;
+  // Sizes that need no scratch do not look the array up, so they never make
+  // the runtime place it in device memory.
+  void *ws = nullptr;
+  if (need > 0) {
+    ws = scratch_on_current_device();
+    if (ws == nullptr) return RA_ERR_CUDA;
+  }
   // Every scratch byte factored_attn reads it has first written in the same
   // call, so nothing is cleared here.
   return factored_attn(q, k, v, out_s, lse_s, out_t, lse_t, B, H, T, N, d, P, ws,
-                       RA_STATIC_SCRATCH_BYTES, stream);
+                       need > 0 ? RA_STATIC_SCRATCH_BYTES : 0, stream);
 }

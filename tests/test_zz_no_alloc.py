@@ -100,3 +100,54 @@ def test_static_scratch_refuses_sizes_beyond_its_limit():
                                          p(lse.data_ptr()), B, H, T, N, d, P,
                                          p(torch.cuda.current_stream().cuda_stream))
     assert rc == -6  # RA_ERR_WORKSPACE
+
+
+CHILD = r"""
+import sys
+sys.path.insert(0, {root!r})
+import torch
+import ring_attention_attn_gb300 as ra
+
+def free():
+    torch.cuda.synchronize()
+    return torch.cuda.mem_get_info()[0]
+
+def args(T, N, d=64):
+    S = T * N
+    q, k, v = (torch.randn(1, 2, S, d, device="cuda").bfloat16() for _ in range(3))
+    outs = (torch.empty_like(q), torch.empty(1, 2, S, device="cuda"),
+            torch.empty_like(q), torch.empty(1, 2, S, device="cuda"))
+    return q, k, v, outs
+
+small = args(8, 50)    # T / P = 2 frames per chunk: no scratch
+big = args(260, 3)     # T / P = 130: the scratch is used
+# the attention kernels (and the workspace version's buffers) first
+ra.factored_attn(*small[:3], 8, 50, 4, outs=small[3])
+ra.factored_attn(*big[:3], 260, 3, 2, outs=big[3])
+f0 = free()
+ra.factored_attn_static(*small[:3], 8, 50, 4, small[3])
+f1 = free()
+ra.factored_attn_static(*big[:3], 260, 3, 2, big[3])
+f2 = free()
+assert ra.ra_get_status() == 0
+print(f0 - f1, f1 - f2)
+"""
+
+
+def test_scratch_is_placed_only_by_calls_that_need_it():
+    """Under the runtime's default lazy loading, a call whose rank chunks fit
+    one tile does not make the 64 MiB array resident; the first call that
+    needs scratch does.  Run in a fresh process, so that no earlier call in
+    this session has placed the array already."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, CUDA_MODULE_LOADING="LAZY")
+    r = subprocess.run([sys.executable, "-c", CHILD.format(root=root)], env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    no_scratch, with_scratch = (int(x) for x in r.stdout.split()[-2:])
+    mib = 1 << 20
+    assert no_scratch < 16 * mib, no_scratch
+    assert with_scratch >= 60 * mib, with_scratch
