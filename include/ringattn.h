@@ -224,9 +224,11 @@ int lse_merge(const float *o_parts, const float *lse_parts, int n, int64_t rows,
  *            together may share a tile (12-frame chunks at P = 4 are taken
  *            in pairs): the ring then has fewer, longer steps, and the
  *            result differs only in the rounding order of the exact merge.
- * The two outputs are independent (not chained).  workspace: device memory
- * of at least factored_attn_workspace(...) bytes, 256-byte aligned, owned
- * by the caller and used as scratch by this call only. */
+ * The two outputs are independent (not chained).  workspace: used only when
+ * the rank chunks are longer than 128 frames (T / P > 128); then device
+ * memory of at least factored_attn_workspace(...) bytes, 256-byte aligned,
+ * owned by the caller and used as scratch by this call only, else ignored
+ * (it may be null). */
 int factored_attn(const void *q, const void *k, const void *v, void *out_s, float *lse_s,
                   void *out_t, float *lse_t, int B, int H, int T, int N, int d, int P,
                   void *workspace, size_t ws_bytes, void *stream);
