@@ -282,8 +282,8 @@ def test_rank_step_subrange():
 def test_c5_full_size_every_tile():
     """One rank's 54,000 queries against 432,000 keys: per-step partials +
     lse_merge (the benchmark's launch configuration) and the fused call, on
-    one row of every 128-row query tile of every head (1,688 rows, the lane
-    rotating over all 128 softmax threads) plus the chunk's first and last
+    two rows of every 128-row query tile of every head (3,376 rows, two lane
+    rotations over all 128 softmax threads) plus the chunk's first and last
     rows."""
     w = synth.WORKLOADS["c5"]
     q, k, v = synth.make_qkv(w)
@@ -294,6 +294,7 @@ def test_c5_full_size_every_tile():
     torch.cuda.synchronize()
     assert ra.ra_get_status() == 0
     rows = np.unique(np.concatenate([synth.tile_rows(w.B * w.H, w.L, w.L),
+                                     synth.tile_rows(w.B * w.H, w.L, w.L, salt=61),
                                      oracle.flat_rows(w.B, w.H, w.L, synth.sample_rows(w, 12))]))
     ro, rl = oracle.attention(q, k, v, rows=rows)
     _cmp(o.reshape(-1, w.d)[rows.tolist()], l.reshape(-1)[rows.tolist()], ro, rl)
