@@ -28,7 +28,26 @@ def test_bench_prints_one_contract_line():
     assert d["value"] > 0 and d["ms_per_step"] > 0
     assert d["roofline"]["bound"] == "tensor" and d["roofline"]["achieved"] > 0
     assert d["roofline"]["peak"] > 0
+    # the kernel is timed in steps of tens of milliseconds: the burst peak
+    roof = d["roofline"]
+    assert roof["peak_kind"].startswith("bf16_tflops burst")
+    assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-9
+    assert "clocks" in d["e2e"]
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] == 2 * 3
     assert "sm_mhz" in d["clocks"]
+
+
+def test_all_configs_prints_gpu_beside_oracle_for_every_workload():
+    """bench.py --all-configs: one line per workload with the GPU time and,
+    from the same run, the oracle's time on the host cores."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--all-configs"],
+                       capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.strip()]
+    assert [d["workload"] for d in lines] == ["c1", "c2", "c3", "c4", "c5"]
+    for d in lines:
+        assert d["gpu_ms"] > 0 and d["gpu_tflops"] > 0
+        o = d["oracle"]
+        assert o["seconds"] > 0 and o["cores"] >= 1 and o["kind"] == "oracle" and o["sample"]
