@@ -75,7 +75,7 @@ struct Cfg {
   static constexpr int kOffKV = 2 * kQTile;
   static constexpr int kOffBar = kOffKV + kSlots * kKVTile;
   static constexpr int kBarBytes = 512;
-  static_assert(8 * (9 + 2 * kSlots + 2) <= 496, "barriers overlap the TMEM slot");
+  static_assert(8 * (9 + 2 * kSlots + 6) <= 496, "barriers overlap the TMEM slot");
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
 };
 
@@ -96,12 +96,29 @@ template <int D>
 __device__ __forceinline__ int bar_xchg() { return kBarKVFull + 2 * Cfg<D>::kSlots; }
 template <int D>
 __device__ __forceinline__ int bar_ofree() { return kBarKVFull + 2 * Cfg<D>::kSlots + 1; }
+// Split units at d = 64 keep three S tiles in tensor memory, and S_full and
+// P_full belong to the S buffer instead of the warpgroup (a warpgroup may
+// finish its next tile before the MMA warp has seen this one's P): the third
+// buffer's S_full and P_full, and per warpgroup "its last PV has completed"
+// (for the rare O rescale, which may no longer assume it).
+template <int D>
+__device__ __forceinline__ int bar_sfull2() { return kBarKVFull + 2 * Cfg<D>::kSlots + 2; }
+template <int D>
+__device__ __forceinline__ int bar_pvdone(int wg) { return kBarKVFull + 2 * Cfg<D>::kSlots + 3 + wg; }
+template <int D>
+__device__ __forceinline__ int bar_pfull2() { return kBarKVFull + 2 * Cfg<D>::kSlots + 5; }
 constexpr int kTmemSlotOff = 496;
 constexpr int kAbortOff = 500;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns of S_i and O_i.
 __device__ __forceinline__ uint32_t col_s(int i) { return static_cast<uint32_t>(i) * 128u; }
 __device__ __forceinline__ uint32_t col_o(int i) { return 256u + static_cast<uint32_t>(i) * 128u; }
+// With three S tiles (split units, d = 64): S_0..S_2 at [0,384), O_0 at
+// [384,448), O_1 at [448,512).
+template <bool S3>
+__device__ __forceinline__ uint32_t col_o_v(int i) {
+  return S3 ? 384u + static_cast<uint32_t>(i) * 64u : col_o(i);
+}
 
 struct Unit {
   int bh, g, rank, s_lo, s_hi, pair, part;
@@ -113,12 +130,33 @@ struct Unit {
 // its units cost about half of the others; they are numbered last so that
 // the block scheduler, which hands out CTAs in index order, packs them into
 // the final, partial wave (longest units first).
-template <bool REM, bool SPLIT>
+template <bool REM, bool SPLIT, bool CAUSAL>
 __device__ __forceinline__ Unit decode_unit(const AttnParams &p, int u) {
   Unit w;
   w.rem = false;
+  if (SPLIT && CAUSAL) {
+    // Causal split units (one query tile each) are numbered longest first:
+    // the rank chunks' last query tiles of every head before their first
+    // ones (in both zigzag halves a tile's visible key tiles grow with its
+    // row), so that the block scheduler starts the longest in the first wave.
+    const int nbg = p.BH * p.G;
+    const int bhg = u % nbg;
+    u /= nbg;
+    w.part = u % p.n_stepgroups;
+    u /= p.n_stepgroups;
+    const int ri = u % p.n_ranks;
+    w.pair = p.n_pairs - 1 - u / p.n_ranks;
+    w.g = bhg % p.G;
+    w.bh = bhg / p.G;
+    w.rank = p.rank_begin + (p.pack_ranks ? 2 * ri : ri);
+    w.s_lo = p.step_begin + w.part * p.steps_per_group;
+    w.s_hi = w.s_lo + p.steps_per_group;
+    w.q_row0 = static_cast<int64_t>(w.bh) * p.q_rows_bh + static_cast<int64_t>(w.g) * p.q_rows_g +
+               static_cast<int64_t>(ri) * (p.q_rank_stride ? p.q_rank_stride : p.L);
+    return w;
+  }
   int np = p.n_pairs, pair_base = 0;
-  // (Split units hold one query tile each: all cost alike, no reordering.)
+  // (Non-causal split units hold one query tile each: all cost alike.)
   if (!SPLIT && p.n_pairs > 1 && p.L - static_cast<int64_t>(p.n_pairs - 1) * 2 * kBM <= kBM) {
     const int heavy = (p.n_pairs - 1) * p.n_stepgroups * p.n_ranks * p.G * p.BH;
     if (u < heavy) {
@@ -205,7 +243,7 @@ struct UnitGeo {
 template <bool CAUSAL, bool REM, bool SPLIT = false>
 __device__ __forceinline__ UnitGeo unit_geo(const AttnParams &p, int u) {
   UnitGeo g;
-  g.w = decode_unit<REM, SPLIT>(p, u);
+  g.w = decode_unit<REM, SPLIT, CAUSAL>(p, u);
   // Split units: "pair" counts single query tiles and there is no tile 1.
   constexpr int kRows = SPLIT ? kBM : 2 * kBM;
   g.pair_row0 = static_cast<int64_t>(g.w.pair) * kRows;
@@ -233,6 +271,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kPack = PK == 1 || PK == 2;
   constexpr bool kSplit = PK == 3;
   static_assert(!kSplit || (!OUT_F32 && !REM), "split units: bf16 output, no stacked rows");
+  // Non-causal split units at d = 64 ring three S tiles: S of tile t + 3 is
+  // issued after PV of tile t, so a warpgroup's next S is usually complete
+  // when its softmax of this tile ends (with two, each warpgroup waits a
+  // PV + QK^T round trip per tile).  Tile t uses S buffer (T + t) mod 3, T
+  // the tiles of the CTA's earlier units.  (Causal rows rescale O more
+  // often, and each rescale must then wait for the warpgroup's last PV:
+  // measured slower there.)
+  constexpr bool kS3 = kSplit && D == 64 && !CAUSAL;
   // REM: launches with packed remainders (rem_pack > 0), non-causal row
   // tiles only.
   static_assert(!REM || (PK == 0 && !CAUSAL), "packed remainders: non-causal row tiles");
@@ -268,6 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kSplit) {
       mbar_init(bar0 + 8 * bar_xchg<D>(), 256);
       mbar_init(bar0 + 8 * bar_ofree<D>(), 256);
+    }
+    if (kS3) {
+      mbar_init(bar0 + 8 * bar_sfull2<D>(), 1);
+      mbar_init(bar0 + 8 * bar_pfull2<D>(), 128);
+      for (int i = 0; i < 2; ++i) mbar_init(bar0 + 8 * bar_pvdone<D>(i), 1);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -444,6 +495,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_pv(tmem + col_o(i), tmem + col_s(i),
                  dv0 + static_cast<uint64_t>(slot * (C::kKVTile >> 4)), idesc_o, acc);
       };
+      // S_full barrier of S buffer b.
+      auto sfull = [&](int b) -> uint32_t {
+        return bar0 + 8 * (b < 2 ? kBarSFull + b : bar_sfull2<D>());
+      };
       int it = 0;          // K/V slot sequence: K_j at 2j, V_j at 2j+1 of each unit
       int n_loaded = 0;    // Q pairs consumed
       int jt[2] = {0, 0};  // tiles handed to each softmax warpgroup so far
@@ -451,8 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kSplit) {
         // Split units: visible key tile t of the unit goes to warpgroup t % 2;
         // both S_i read the one query tile.  S of tile t + 2 is issued right
-        // after PV of tile t (it overwrites the same TMEM columns).
+        // after PV of tile t (it overwrites the same TMEM columns); with three
+        // S buffers (d = 64), S of tile t + 3.
         int n_units_done = 0;  // units with at least one tile (O_done / O_free phases)
+        int t_base = 0;        // tiles of earlier units (S buffer rotation, three buffers)
         for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
           const UnitGeo g = unit_geo<CAUSAL, kRem, kSplit>(p, u);
           const Unit &w = g.w;
@@ -471,10 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                            abort_flag))
               return false;
             tc_fence_after();
+            if (kS3) i = (t_base + ns) % 3;
             issue_qk<D>(tmem + col_s(i), dq[0],
                         dk0 + static_cast<uint64_t>((seq % C::kSlots) * (C::kKVTile >> 4)),
                         idesc_s);
-            mma_commit_e(bar0 + 8 * (kBarSFull + i));
+            mma_commit_e(sfull(i));
             mma_commit_e(kv_empty0 + 8 * (seq % C::kSlots));
             ++ns;
             ++ts.t;
@@ -484,7 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ts.valid(w)) mma_commit_e(bar0 + 8 * kBarQEmpty);
             return true;
           };
-          ok = issue_next_s(0) && (!ts.valid(w) || issue_next_s(1));
+          ok = issue_next_s(0) && (!ts.valid(w) || issue_next_s(1)) &&
+               (!kS3 || !ts.valid(w) || issue_next_s(2));
           issued = true;
           for (int t = 0; ok && t < ns; ++t) {
             const int i = t & 1;
@@ -492,9 +551,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = mbar_wait(kv_full0 + 8 * (seq_v % C::kSlots), (seq_v / C::kSlots) & 1, wd,
                                  abort_flag)))
               break;
-            if (!(ok = mbar_wait(bar0 + 8 * (kBarPFull + i), (jt[i] + (t >> 1)) & 1, wd,
-                                 abort_flag)))
-              break;
+            {
+              uint32_t p_bar = bar0 + 8 * (kBarPFull + i), p_par = (jt[i] + (t >> 1)) & 1;
+              if (kS3) {
+                const int gt = t_base + t, b = gt % 3;
+                p_bar = bar0 + 8 * (b < 2 ? kBarPFull + b : bar_pfull2<D>());
+                p_par = (gt / 3) & 1;
+              }
+              if (!(ok = mbar_wait(p_bar, p_par, wd, abort_flag))) break;
+            }
             // The first PV of a unit overwrites O_i: both warpgroups must
             // have read the previous unit's accumulators.
             if (t < 2 && n_units_done > 0 &&
@@ -502,12 +567,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  abort_flag)))
               break;
             tc_fence_after();
-            issue_o(i, seq_v % C::kSlots, t >= 2);
+            if (kS3) {
+              // P_t sits in S buffer (t_base + t) mod 3; S of tile t + 3
+              // takes that buffer after this PV.
+              issue_pv(tmem + col_o_v<kS3>(i), tmem + col_s((t_base + t) % 3),
+                       dv0 + static_cast<uint64_t>((seq_v % C::kSlots) * (C::kKVTile >> 4)),
+                       idesc_o, t >= 2);
+              mma_commit_e(bar0 + 8 * bar_pvdone<D>(i));
+            } else {
+              issue_o(i, seq_v % C::kSlots, t >= 2);
+            }
             mma_commit_e(kv_empty0 + 8 * (seq_v % C::kSlots));
             if (ts.valid(w) && !(ok = issue_next_s(i))) break;
           }
           if (!ok) break;
           it = base + 2 * ns;
+          t_base += ns;
           for (int i = 0; i < 2; ++i) mma_commit_e(bar0 + 8 * (kBarODone + i));
           jt[0] += (ns + 1) >> 1;
           jt[1] += ns >> 1;
@@ -596,11 +671,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_bits = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_bits + col_s(wg);
-    const uint32_t tO = tmem + lane_bits + col_o(wg);
-    // This thread's TMEM lanes and columns: its S tile and O accumulator.
-    (void)RA_IN_BOUNDS(wg < 2 && row < kBM && col_s(wg) + kBN <= kTmemCols &&
-                           col_o(wg) + D <= kTmemCols && (col_o(wg) >= col_s(1) + kBN),
+    uint32_t tS = tmem + lane_bits + col_s(wg);  // per tile with three S buffers
+    const uint32_t tO = tmem + lane_bits + col_o_v<kS3>(wg);
+    // This thread's TMEM lanes and columns: its S tiles and O accumulator.
+    (void)RA_IN_BOUNDS(wg < 2 && row < kBM && col_s(kS3 ? 2 : 1) + kBN <= col_o_v<kS3>(0) &&
+                           col_o_v<kS3>(wg) + D <= kTmemCols &&
+                           (col_o_v<kS3>(1) >= col_o_v<kS3>(0) + D),
                        wd.status);
     const float sl2 = p.scale_log2;
     // Rows start 32-byte aligned when the output and its part stride are
@@ -610,6 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          31u) == 0;
     int jt = 0;      // tiles of this warpgroup so far (S_full / P_full phases)
     int n_done = 0;  // units whose O this warpgroup has read (O_done phases)
+    int t_base = 0;  // tiles of earlier units (three S buffers)
     // The next unit's geometry is decoded while the last PV of the current
     // one runs, off the path from this unit's epilogue to the next S.
     UnitGeo g_next = unit_geo<CAUSAL, kRem, kSplit>(p, blockIdx.x);
@@ -665,8 +742,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           ti.settle<CAUSAL>(p, w, n_t, g.gq_max);
           continue;
         }
-        const bool ok = __all_sync(
-            0xffffffffu, mbar_wait(bar0 + 8 * (kBarSFull + wg), (jt + j) & 1, wd, abort_flag));
+        uint32_t s_bar = bar0 + 8 * (kBarSFull + wg), s_par = (jt + j) & 1;
+        uint32_t p_bar = bar0 + 8 * (kBarPFull + wg);
+        if (kS3) {
+          // Tile tv's S buffer b = (t_base + tv) mod 3, used (t_base + tv) / 3
+          // times before.
+          const int gt = t_base + tv, b = gt % 3;
+          tS = tmem + lane_bits + col_s(b);
+          s_bar = bar0 + 8 * (b < 2 ? kBarSFull + b : bar_sfull2<D>());
+          s_par = (gt / 3) & 1;
+          p_bar = bar0 + 8 * (b < 2 ? kBarPFull + b : bar_pfull2<D>());
+        }
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(s_bar, s_par, wd, abort_flag));
         if (!ok) break;
         tc_fence_after();
         if constexpr (PK == 2) {
@@ -806,6 +893,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             lr = lr * alpha + (rqs.x + rqs.y);
           }
           if (__any_sync(0xffffffffu, rescale)) {
+            // Three S buffers: this warpgroup's previous PV (tile tv - 2) may
+            // still be accumulating into O.
+            if (kS3 && !__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * bar_pvdone<D>(wg),
+                                                           (jt + j - 1) & 1, wd, abort_flag)))
+              break;
+            if (kS3) tc_fence_after();
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
               float o[32];
@@ -819,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar0 + 8 * (kBarPFull + wg));
+        mbar_arrive(p_bar);
         ++j;
         ++tv;
         ++ti.t;
@@ -837,6 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // by unit), O0 and O1 read from tensor memory; warpgroup i writes
         // columns [i D/2, (i+1) D/2) of the row.
         jt += j;
+        t_base += tv;
         if (tv == 0) continue;  // no visible key tile: the MMA warp skipped the unit too
         float *xb = reinterpret_cast<float *>(smem + C::kOffQ1) + (n_done & 1) * (4 * kBM);
         xb[(wg * kBM + row) * 2] = m_ref;
@@ -864,7 +958,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row_valid && !RA_IN_BOUNDS(orow >= 0 && orow < p.chk_out_rows, wd.status))
           row_valid = false;
         __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * D;
-        const uint32_t tO0 = tmem + lane_bits + col_o(0), tO1 = tmem + lane_bits + col_o(1);
+        const uint32_t tO0 = tmem + lane_bits + col_o_v<kS3>(0);
+        const uint32_t tO1 = tmem + lane_bits + col_o_v<kS3>(1);
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc) {
           const int c = wg * (D / 64) + cc;

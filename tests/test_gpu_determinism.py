@@ -51,13 +51,17 @@ def test_overlapped_ring_and_backward_are_deterministic():
     _same_every_time(lambda: ra.ring_attn_bwd(q, k, v, o, lse, do, P))
 
 
-@pytest.mark.parametrize("causal,d", [(True, 64), (False, 128)])
-def test_split_units_are_deterministic(causal, d):
+@pytest.mark.parametrize("causal,d,H,S", [(True, 64, 4, 4096), (False, 128, 4, 4096),
+                                         (True, 64, 18, 2048), (False, 128, 18, 2048)])
+def test_split_units_are_deterministic(causal, d, H, S):
     """Launches of fewer query-tile pairs than SMs run as split units (the two
     softmax warpgroups alternate key tiles and merge through shared memory):
-    the exchange and the "both accumulators read" barrier must leave no race."""
-    g = torch.Generator(device="cuda").manual_seed(8 + d)
-    q, k, v = (_rnd(g, 1, 4, 4096, d) for _ in range(3))
+    the exchange and the "both accumulators read" barrier must leave no race.
+    With at most as many split units as SMs (H = 4) each runs on a CTA pair,
+    whose second CTA hands its state over in the first CTA's K/V slots: the
+    two barriers of that hand-over must leave none either."""
+    g = torch.Generator(device="cuda").manual_seed(8 + d + H)
+    q, k, v = (_rnd(g, 1, H, S, d) for _ in range(3))
     if causal:
         q, k, v = (ra.ra_cp_shard(x, 2, 1) for x in (q, k, v))
     _same_every_time(lambda: ra.ring_attn_fwd(q, k, v, 2, causal=causal))

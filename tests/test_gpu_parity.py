@@ -130,18 +130,43 @@ CASES = [
     (2, 1, 2112, 64, 8, False),   # 264-row chunks: 8 x 8 rows
     (1, 1, 656, 128, 2, False),   # 328-row chunks: 2 x 72 rows do not fit
     # at least as many query-tile pairs as SMs: pair units (fewer run as split
-    # units, one query tile each, key tiles alternating between warpgroups)
+    # units, one query tile each, key tiles alternating between warpgroups;
+    # when the split units fit the 152 SMs, each runs on a pair of CTAs that
+    # take alternate key tiles)
     (1, 40, 2048, 64, 2, True),
     (1, 24, 2048, 128, 4, True),
     (1, 40, 2048, 128, 2, False),
-    (1, 3, 384, 64, 1, False),    # split units of 3 key tiles: odd count per warpgroup
-    (1, 2, 128, 128, 1, True),    # one key tile: the second warpgroup meets none
+    (1, 18, 2048, 64, 2, True),   # 144 pairs, 288 split units: one CTA each
+    (1, 18, 2048, 128, 2, False),
+    (1, 3, 384, 64, 1, False),    # 3 key tiles: CTA 0 takes 2 (one per warpgroup), CTA 1 one
+    (1, 2, 128, 128, 1, True),    # one key tile: the second CTA meets none
+    (1, 5, 1920, 64, 3, True),    # causal 640-row chunks: 1 to 15 key tiles per query tile
 ]
 
 
 @pytest.mark.parametrize("B,H,S,d,P,causal", CASES)
 def test_ring_small_cases(B, H, S, d, P, causal):
     q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=S * 7 + d + P)
+    o, l = _run_ring(q, k, v, P, causal)
+    ro, rl = oracle.attention(q, k, v, causal=causal)
+    _cmp(o, l, ro, rl)
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (128, False), (64, True)])
+def test_ring_rescale_every_tile(d, causal):
+    """Scores that rise tile by tile: channel 0 holds 4 in every query and
+    round(6.5 t sqrt(d) / 4) in the keys of key tile t, so each tile's scores
+    sit ~6.5 (9.4 in log2 units) above the previous tile's while their spread
+    within the tile stays that of the random channels.  Row maxima then jump
+    past the lazy-rescale threshold (2^8) at nearly every tile, and O is
+    rescaled each time.  Split units (fewer query-tile pairs than SMs), where
+    at d = 64 without the mask three S buffers let a warpgroup reach a tile
+    before its previous PV is issued."""
+    B, H, S, P = 1, 2, 1024, 1
+    q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=77 + d + causal)
+    q, k = q.clone(), k.clone()
+    q[..., 0] = 4.0
+    k[..., 0] = (torch.arange(S) // 128).float().mul(6.5 * d ** 0.5 / 4).round().bfloat16()
     o, l = _run_ring(q, k, v, P, causal)
     ro, rl = oracle.attention(q, k, v, causal=causal)
     _cmp(o, l, ro, rl)
