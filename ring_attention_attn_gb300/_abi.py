@@ -50,6 +50,8 @@ class RingAttnError(RuntimeError):
 def lib():
     """The loaded library (raises if it has not been built)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -108,10 +110,23 @@ def _check(code: int, where: str):
         raise RingAttnError(code, where)
 
 
+_raw_stream = None
+
+
 def _stream(stream=None):
+    """The given stream, else the current torch stream of the current device
+    (read as a raw handle: building a torch Stream object per call costs
+    microseconds)."""
+    global _raw_stream
     import torch
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _raw_stream is None:
+        get = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        dev = getattr(torch._C, "_cuda_getDevice", None)
+        _raw_stream = ((lambda: get(dev())) if get is not None and dev is not None
+                       else (lambda: torch.cuda.current_stream().cuda_stream))
+    return ctypes.c_void_p(_raw_stream())
 
 
 def _dev(t, dtype, name):
