@@ -5,9 +5,13 @@ resident in HBM, 3 warm-up calls, then `reps` calls back to back between two
 events: the mean, launch gaps hidden as in a real pipeline) and prints one
 JSON line per path with its algorithmic throughput and roofline fraction
 against MEASURED_PEAKS.json (bf16 dense burst peak for contractions, HBM copy
-bandwidth for permutations and merges).  Usage:
+bandwidth for permutations and merges).  With --graph each line also
+carries the per-call time of the same calls captured in one CUDA graph and
+replayed (`graph_ms`: no host submission between calls, so for the short
+workloads it is the device time that back-to-back calls hide behind the
+host's per-call cost).  Usage:
 
-    python -m ring_attention_attn_gb300.measure [--path NAME ...] [--reps N]
+    python -m ring_attention_attn_gb300.measure [--path NAME ...] [--reps N] [--graph]
 
 Paths: shard, transpose, merge, ring_c1, ring_c2, ring_c3, rank_c5, factored_c4,
 factored_c4_unfolded, overlap_c3, ulysses_c3, allgather_c3, reducescatter_c3, bwd_c3.
@@ -31,6 +35,9 @@ def _peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
+_GRAPH = {"on": False, "ms": None}
+
+
 def _time(fn, reps):
     import torch
     for _ in range(3):
@@ -43,7 +50,38 @@ def _time(fn, reps):
         fn()
     e1.record()
     torch.cuda.synchronize()
+    _GRAPH["ms"] = _time_graph(fn, reps) if _GRAPH["on"] else None
     return e0.elapsed_time(e1) / reps
+
+
+def _time_graph(fn, reps):
+    """Mean per-call time of `reps` calls captured in one CUDA graph and
+    replayed three times; None when the calls cannot be captured."""
+    import torch
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(3):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (3 * reps)
+    except RuntimeError:
+        torch.cuda.synchronize()
+        return None
 
 
 def _rand(shape, gen):
@@ -51,8 +89,9 @@ def _rand(shape, gen):
     return torch.randn(shape, device="cuda", generator=gen).bfloat16()
 
 
-def run(paths, reps):
+def run(paths, reps, graph=False):
     import torch
+    _GRAPH["on"] = graph
 
     sys.path.insert(0, ROOT)
     import ring_attention_attn_gb300 as ra
@@ -69,6 +108,10 @@ def run(paths, reps):
             val, peak = work / ms / 1e6, pk["hbm_gbs"]
         line = {"path": path, "ms": ms, "achieved": val, "unit": unit, "bound": bound,
                 "peak": peak, "frac": val / peak, "peak_source": pk["source"], **extra}
+        if _GRAPH["on"]:
+            gms = _GRAPH["ms"]
+            line["graph_ms"] = gms
+            line["graph_achieved"] = (val * ms / gms) if gms else None
         print(json.dumps(line), flush=True)
         out.append(line)
 
@@ -173,5 +216,7 @@ if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--path", nargs="*", default=ALL)
     ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the calls under CUDA-graph replay (graph_ms)")
     a = ap.parse_args()
-    run(a.path, a.reps)
+    run(a.path, a.reps, a.graph)

@@ -51,3 +51,20 @@ def test_all_configs_prints_gpu_beside_oracle_for_every_workload():
         assert d["gpu_ms"] > 0 and d["gpu_tflops"] > 0
         o = d["oracle"]
         assert o["seconds"] > 0 and o["cores"] >= 1 and o["kind"] == "oracle" and o["sample"]
+
+
+def test_measure_reports_graph_replay_times():
+    """measure.py --graph: each line carries the per-call time of the same
+    calls replayed from one CUDA graph; for the 1,024-token launch the host
+    submits slower than the device runs, so the replay is the faster one."""
+    r = subprocess.run([sys.executable, "-m", "ring_attention_attn_gb300.measure", "--path",
+                        "ring_c1", "merge", "--reps", "10", "--graph"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.strip()]
+    assert [l["path"] for l in lines] == ["ring_c1", "merge"]
+    for l in lines:
+        assert l["ms"] > 0 and l["graph_ms"] is not None and l["graph_ms"] > 0
+        assert abs(l["graph_achieved"] - l["achieved"] * l["ms"] / l["graph_ms"]) < 1e-6 * l[
+            "graph_achieved"]
+    assert lines[0]["graph_ms"] < lines[0]["ms"]
