@@ -122,8 +122,14 @@ int ring_attn_fwd_rank(const void *q_local, const void *k, const void *v, void *
  * last rows (as in ring_attn_fwd) read rank 0's current block at every step,
  * so each rank's last rows still meet every block once.
  * comm_stream may equal stream (copies then serialise with compute).
+ * comm_stream NULL: no copy calls and no events; each step's launch itself
+ * copies the blocks the next step reads (the same 2P ring sends), with warps
+ * that the attention leaves idle, and the stream orders the steps.  On one
+ * GPU this is the form that overlaps: a device-to-device copy runs on the
+ * SMs and cannot start beside a launch that holds all of them.
  * workspace: >= ring_attn_fwd_overlap_workspace(...) bytes, 256-byte aligned,
- * used by this call only.  Events are created and released internally. */
+ * used by this call only.  Events (comm_stream not NULL) are created and
+ * released internally. */
 int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out, float *lse,
                           int B, int H, int64_t S, int d, int P, int causal, void *workspace,
                           size_t ws_bytes, void *stream, void *comm_stream);

@@ -227,7 +227,9 @@ def ring_attn_fwd_overlap_workspace(B: int, H: int, S: int, d: int, P: int) -> i
 def ring_attn_fwd_overlap(q, k, v, P: int, causal: bool = False, workspace=None, out=None,
                           lse=None, stream=None, comm_stream=None):
     """ring_attn_fwd with the ring's K/V exchange done as device copies on
-    `comm_stream`, overlapped with each step's attention (sharded order)."""
+    `comm_stream`, overlapped with each step's attention (sharded order).
+    comm_stream None: each step's launch copies the next step's blocks itself
+    (no copy calls, no events)."""
     import torch
     B, H, S, d = q.shape
     need = ring_attn_fwd_overlap_workspace(B, H, S, d, P)

@@ -263,7 +263,10 @@ int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out
   if (!workspace || ws_bytes < need) return RA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RA_ERR_ALIGN;
   cudaStream_t cs = as_stream(stream);
-  cudaStream_t xs = comm_stream ? as_stream(comm_stream) : cs;
+  // Without a comm stream the exchange runs inside the step launches (their
+  // idle warps copy the next step's blocks), ordered by the stream alone.
+  const bool in_launch = comm_stream == nullptr;
+  cudaStream_t xs = in_launch ? cs : as_stream(comm_stream);
   ra::WatchdogParams wd;
   if (!watchdog(&wd)) return fail_cuda(cudaGetLastError());
 
@@ -277,24 +280,26 @@ int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out
   float *l_parts = reinterpret_cast<float *>(
       ws + 4 * buf_bytes + ovl_part(static_cast<size_t>(P) * BH * S * d * 4));
 
-  cudaEvent_t copied[2], consumed[2];
+  cudaEvent_t copied[2] = {}, consumed[2] = {};
   cudaError_t e = cudaSuccess;
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < 2 && !in_launch; ++i) {
     if ((e = cudaEventCreateWithFlags(&copied[i], cudaEventDisableTiming)) != cudaSuccess)
       return fail_cuda(e);
     if ((e = cudaEventCreateWithFlags(&consumed[i], cudaEventDisableTiming)) != cudaSuccess)
       return fail_cuda(e);
   }
   // The comm stream may not start before inputs written on `stream` are ready.
-  cudaEvent_t start;
-  if ((e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming)) != cudaSuccess)
-    return fail_cuda(e);
-  e = cudaEventRecord(start, cs);
-  if (e == cudaSuccess && xs != cs) e = cudaStreamWaitEvent(xs, start, 0);
+  cudaEvent_t start = nullptr;
+  if (!in_launch) {
+    if ((e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming)) != cudaSuccess)
+      return fail_cuda(e);
+    e = cudaEventRecord(start, cs);
+    if (e == cudaSuccess && xs != cs) e = cudaStreamWaitEvent(xs, start, 0);
+  }
 
   for (int s = 0; s < P && e == cudaSuccess; ++s) {
     // ---- comm: ring send for step s + 1 (rank r receives rank r-1's block).
-    if (s + 1 < P) {
+    if (!in_launch && s + 1 < P) {
       const int nb = (s + 1) & 1;
       if (s >= 1) e = cudaStreamWaitEvent(xs, consumed[nb], 0);  // step s-1 read it
       for (int r = 0; r < P && e == cudaSuccess; ++r) {
@@ -317,7 +322,7 @@ int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out
     }
     if (e != cudaSuccess) break;
     // ---- compute: step s for every rank, from its current buffer.
-    if (s >= 1) e = cudaStreamWaitEvent(cs, copied[s & 1], 0);
+    if (!in_launch && s >= 1) e = cudaStreamWaitEvent(cs, copied[s & 1], 0);
     if (e != cudaSuccess) break;
     ra::AttnParams p{};
     p.BH = static_cast<int>(BH);
@@ -349,16 +354,36 @@ int ring_attn_fwd_overlap(const void *q, const void *k, const void *v, void *out
       ks = kb[s & 1];
       vs = vb[s & 1];
     }
+    if (in_launch && s + 1 < P) {
+      // The same ring send as the copies above, done by this launch: rank r's
+      // next buffer receives rank r - 1's current block (step 0: the inputs,
+      // a head pitch of S rows).
+      const int nb = (s + 1) & 1;
+      p.x_on = 1;
+      p.x_ranks = P;
+      p.x_bh = static_cast<int>(BH);
+      p.xk_src = static_cast<const uint8_t *>(s == 0 ? k : kb[s & 1]);
+      p.xv_src = static_cast<const uint8_t *>(s == 0 ? v : vb[s & 1]);
+      p.xk_dst = kb[nb];
+      p.xv_dst = vb[nb];
+      p.x_row_bytes = L * d * 2;
+      p.x_src_rank = s == 0 ? L * d * 2 : static_cast<int64_t>(blk_bytes);
+      p.x_src_head = s == 0 ? S * d * 2 : L * d * 2;
+      p.x_dst_rank = static_cast<int64_t>(blk_bytes);
+      p.x_dst_head = L * d * 2;
+      p.x_src_span = s == 0 ? BH * S * d * 2 : static_cast<int64_t>(P) * blk_bytes;
+      p.x_dst_span = static_cast<int64_t>(P) * blk_bytes;
+    }
     e = ra::launch_ring_attn(q, BH * S, ks, vs, kv_rows, d, true, p, cs);
-    if (e == cudaSuccess && s >= 1) e = cudaEventRecord(consumed[s & 1], cs);
+    if (e == cudaSuccess && !in_launch && s >= 1) e = cudaEventRecord(consumed[s & 1], cs);
   }
   if (e == cudaSuccess)
     e = ra::launch_lse_merge(o_parts, l_parts, P, BH * S, d, out, lse, wd.status, cs);
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < 2 && !in_launch; ++i) {
     cudaEventDestroy(copied[i]);
     cudaEventDestroy(consumed[i]);
   }
-  cudaEventDestroy(start);
+  if (start) cudaEventDestroy(start);
   return e == cudaSuccess ? RA_OK : fail_cuda(e);
 }
 

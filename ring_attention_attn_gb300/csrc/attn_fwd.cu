@@ -477,6 +477,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = max(0, it - C::kSlots); i < it; ++i)
         mbar_wait_drain(kv_full0 + 8 * (i % C::kSlots), (i / C::kSlots) & 1, p.wd.limit_ns);
     }
+  } else if (warp == 2 || warp == 3) {
+    // ----------------------------------------------- in-launch ring exchange --
+    // (Overlapped ring without a comm stream: this launch copies the blocks
+    // the next step reads while its other warps compute.  A device copy would
+    // need SMs that the launch holds.)
+    if (p.x_on) {
+      // Work items of up to 64 KB of one row, grid-strided over the CTAs; the
+      // 64 threads keep eight 16-byte loads each in flight.
+      constexpr int kU = 8;
+      constexpr int64_t kChunk = 4096;  // 16-byte pieces per work item
+      const int tid = static_cast<int>(threadIdx.x) - 64;
+      const int64_t per_row = p.x_row_bytes >> 4;
+      const int64_t chunks = (per_row + kChunk - 1) / kChunk;
+      const int64_t rows = static_cast<int64_t>(p.x_ranks) * p.x_bh;
+      const int64_t n_items = 2 * rows * chunks;
+      for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int64_t row2 = item / chunks, c = item - row2 * chunks;
+        const int tsel = row2 >= rows;
+        const int64_t row = row2 - (tsel ? rows : 0);
+        const int r = static_cast<int>(row / p.x_bh);
+        const int64_t h = row - static_cast<int64_t>(r) * p.x_bh;
+        const int from = (r + p.x_ranks - 1) % p.x_ranks;
+        const int64_t so = from * p.x_src_rank + h * p.x_src_head;
+        const int64_t dof = r * p.x_dst_rank + h * p.x_dst_head;
+        const int64_t p0 = c * kChunk, p1 = min64(per_row, p0 + kChunk);
+        if (!RA_IN_BOUNDS(so >= 0 && so + p1 * 16 <= p.x_src_span && dof >= 0 &&
+                              dof + p1 * 16 <= p.x_dst_span,
+                          wd.status))
+          continue;
+        const uint4 *src = reinterpret_cast<const uint4 *>((tsel ? p.xv_src : p.xk_src) + so);
+        uint4 *dst = reinterpret_cast<uint4 *>((tsel ? p.xv_dst : p.xk_dst) + dof);
+        for (int64_t pc = p0 + tid; pc < p1; pc += 64 * kU) {
+          uint4 val[kU];
+#pragma unroll
+          for (int u = 0; u < kU; ++u)
+            if (pc + u * 64 < p1) val[u] = src[pc + u * 64];
+#pragma unroll
+          for (int u = 0; u < kU; ++u)
+            if (pc + u * 64 < p1) dst[pc + u * 64] = val[u];
+        }
+      }
+    }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issue --
     {

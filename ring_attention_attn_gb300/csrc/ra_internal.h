@@ -63,6 +63,16 @@ struct AttnParams {
   // (rank r at tile rows [r * rem_pack, (r + 1) * rem_pack)), meeting the
   // key tiles in the first rank's ring order.
   int rem_pack;
+  // Overlapped ring, exchange inside the launch: when x_on != 0 the CTAs'
+  // otherwise idle warps 2 and 3 copy, for both K and V, every rank r's
+  // next block: x_ranks x x_bh rows of x_row_bytes from
+  // src + ((r - 1) mod x_ranks) * x_src_rank + h * x_src_head to
+  // dst + r * x_dst_rank + h * x_dst_head.  x_src_span / x_dst_span bound
+  // the byte offsets (bounds-checked build).
+  int x_on, x_ranks, x_bh;
+  const uint8_t *xk_src, *xv_src;
+  uint8_t *xk_dst, *xv_dst;
+  int64_t x_src_rank, x_src_head, x_dst_rank, x_dst_head, x_row_bytes, x_src_span, x_dst_span;
   WatchdogParams wd;
   // Extents for the RA_CHECKS build's bounds checks (set by launch_ring_attn):
   // rows of the Q and K/V row matrices, output rows per part, output parts.

@@ -14,7 +14,8 @@ host's per-call cost).  Usage:
     python -m ring_attention_attn_gb300.measure [--path NAME ...] [--reps N] [--graph]
 
 Paths: shard, transpose, merge, ring_c1, ring_c2, ring_c3, rank_c5, factored_c4,
-factored_c4_unfolded, overlap_c3, ulysses_c3, allgather_c3, reducescatter_c3, bwd_c3.
+factored_c4_unfolded, overlap_c3, overlap_c3_stream, ulysses_c3, allgather_c3,
+reducescatter_c3, bwd_c3.
 """
 from __future__ import annotations
 
@@ -170,14 +171,16 @@ def run(paths, reps, graph=False):
             sp, tp = acc.factored_flops(B * H, T, N, d)
             ra.ra_set_temporal_fold(True)
             emit(path, ms, sp + tp, "TFLOP/s", "tensor", spatial_flops=sp, temporal_flops=tp)
-        elif path.endswith("_c3"):
+        elif path.endswith("_c3") or path == "overlap_c3_stream":
             B, H, S, d, P = 1, 24, 14400, 128, 4
             q, k, v = qkv(B, H, S, d)
             fl = acc.attention_flops(B * H, S, S, d)
-            if path == "overlap_c3":
+            if path in ("overlap_c3", "overlap_c3_stream"):
                 ws = torch.empty(ra.ring_attn_fwd_overlap_workspace(B, H, S, d, P),
                                  dtype=torch.uint8, device="cuda")
-                comm = torch.cuda.Stream()
+                # overlap_c3: the exchange inside the step launches (no comm
+                # stream); overlap_c3_stream: device copies on a comm stream
+                comm = torch.cuda.Stream() if path == "overlap_c3_stream" else None
                 ms = _time(lambda: ra.ring_attn_fwd_overlap(q, k, v, P, workspace=ws,
                                                             comm_stream=comm), reps)
                 emit(path, ms, fl, "TFLOP/s", "tensor")
@@ -209,7 +212,8 @@ def run(paths, reps, graph=False):
 
 
 ALL = ["shard", "transpose", "merge", "ring_c1", "ring_c2", "ring_c3", "rank_c5", "factored_c4",
-       "factored_c4_unfolded", "overlap_c3", "ulysses_c3", "allgather_c3", "reducescatter_c3", "bwd_c3"]
+       "factored_c4_unfolded", "overlap_c3", "overlap_c3_stream", "ulysses_c3", "allgather_c3",
+       "reducescatter_c3", "bwd_c3"]
 
 
 if __name__ == "__main__":

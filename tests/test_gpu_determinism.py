@@ -47,6 +47,9 @@ def test_overlapped_ring_and_backward_are_deterministic():
                      device="cuda")
     comm = torch.cuda.Stream()
     _same_every_time(lambda: ra.ring_attn_fwd_overlap(q, k, v, P, workspace=ws, comm_stream=comm))
+    # the exchange inside the step launches: a block copied while the same
+    # launch reads the other buffer
+    _same_every_time(lambda: ra.ring_attn_fwd_overlap(q, k, v, P, workspace=ws))
     o, lse = ra.ring_attn_fwd(q, k, v, P)
     _same_every_time(lambda: ra.ring_attn_bwd(q, k, v, o, lse, do, P))
 

@@ -328,15 +328,21 @@ def test_c5_full_size_every_tile():
 
 
 # ------------------------------------------------- overlapped ring copies --
-@pytest.mark.parametrize("B,H,S,d,P,causal,separate",
-                         [(1, 2, 2048, 128, 4, False, True), (1, 2, 4096, 64, 2, True, True),
-                          (2, 1, 1200, 128, 3, True, False), (1, 3, 1000, 64, 8, False, True),
-                          (1, 2, 1088, 128, 4, False, True)])  # stacked last rows
-def test_overlap_ring_matches_oracle_and_fused(B, H, S, d, P, causal, separate):
+# exchange: "stream" = copies on a comm stream, "same" = copies serialised on
+# the compute stream, "launch" = no comm stream, the step launches copy
+@pytest.mark.parametrize("B,H,S,d,P,causal,exchange",
+                         [(1, 2, 2048, 128, 4, False, "stream"), (1, 2, 4096, 64, 2, True, "stream"),
+                          (2, 1, 1200, 128, 3, True, "same"), (1, 3, 1000, 64, 8, False, "stream"),
+                          (1, 2, 1088, 128, 4, False, "stream"),  # stacked last rows
+                          (1, 2, 2048, 128, 4, False, "launch"), (1, 2, 4096, 64, 2, True, "launch"),
+                          (2, 1, 1200, 128, 3, True, "launch"), (1, 3, 1000, 64, 8, False, "launch"),
+                          (1, 2, 1088, 128, 4, False, "launch")])
+def test_overlap_ring_matches_oracle_and_fused(B, H, S, d, P, causal, exchange):
     layout = 1 if causal else 0
     q, k, v = synth.make_custom((B, H, S, d), (B, H, S, d), seed=S + 11 * P + causal)
     qs, ks, vs = (_shard_host(x, P, layout).cuda() for x in (q, k, v))
-    comm = torch.cuda.Stream() if separate else None
+    comm = {"stream": torch.cuda.Stream(), "same": torch.cuda.current_stream(),
+            "launch": None}[exchange]
     o, l = ra.ring_attn_fwd_overlap(qs, ks, vs, P, causal=causal, comm_stream=comm)
     fo, fl = ra.ring_attn_fwd(qs, ks, vs, P, causal=causal)
     torch.cuda.synchronize()
