@@ -2,7 +2,14 @@
 oracle: ragged chunk lengths, odd head counts, both head sizes, causal and
 not, P from 1 to 8, frame counts around the 16/32/128-row packing limits and
 the folding of short rank chunks, and chunks whose short last rows every
-form (and the backward) stacks into one tile."""
+form (and the backward) stacks into one tile.
+
+Wider sweeps: RA_FUZZ_SCALE multiplies the number of random ring, factored
+and stacked cases (default 1), RA_FUZZ_SEED offsets their seeds (default 0)
+and RA_FUZZ_SMAX bounds the ring sequence length (default 2400), e.g.
+RA_FUZZ_SCALE=100 RA_FUZZ_SEED=1 RA_FUZZ_SMAX=6000 pytest tests/test_gpu_fuzz.py."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -23,6 +30,10 @@ LSE_TOL = 1e-3
 # bf16 unit of |O| on top of the bound.
 O_REL = 2.0 ** -8
 
+SCALE = int(os.environ.get("RA_FUZZ_SCALE", "1"))
+SEED = int(os.environ.get("RA_FUZZ_SEED", "0"))
+SMAX = int(os.environ.get("RA_FUZZ_SMAX", "2400"))
+
 
 def _cmp(o_gpu, l_gpu, o_ref, l_ref):
     o = o_gpu.double().cpu().numpy().reshape(o_ref.shape)
@@ -36,13 +47,13 @@ def _cmp(o_gpu, l_gpu, o_ref, l_ref):
 
 
 def _ring_cases():
-    rng = np.random.default_rng(20261202)
+    rng = np.random.default_rng(20261202 + SEED)
     cases = []
-    while len(cases) < 24:
+    while len(cases) < 24 * SCALE:
         P = int(rng.integers(1, 9))
         causal = bool(rng.integers(0, 2))
         unit = 2 * P if causal else P
-        S = unit * int(rng.integers(1, max(2, 2400 // unit)))
+        S = unit * int(rng.integers(1, max(2, SMAX // unit)))
         cases.append((1, int(rng.integers(1, 4)), S, int(rng.choice([64, 128])), P, causal,
                       int(rng.integers(0, 1 << 30))))
     return cases
@@ -65,11 +76,15 @@ def test_ring_random_shapes(B, H, S, d, P, causal, seed):
 
 
 def _factored_cases():
-    rng = np.random.default_rng(4242)
+    rng = np.random.default_rng(4242 + SEED)
     cases = []
     # (8, 8), (36, 6), (48, 8), (60, 4): short chunks that fold by 4, 3, 4, 2.
-    for T, P in [(4, 4), (15, 5), (16, 1), (17, 1), (32, 2), (33, 3), (64, 2), (96, 3), (128, 1),
-                 (130, 2), (8, 8), (36, 6), (48, 8), (60, 4)]:
+    tp = [(4, 4), (15, 5), (16, 1), (17, 1), (32, 2), (33, 3), (64, 2), (96, 3), (128, 1),
+          (130, 2), (8, 8), (36, 6), (48, 8), (60, 4)]
+    while len(tp) < 14 * SCALE:
+        P = int(rng.choice([1, 2, 3, 4, 5, 6, 8]))
+        tp.append((P * int(rng.integers(1, 40)), P))
+    for T, P in tp:
         N = int(rng.integers(3, 60))
         cases.append((1, int(rng.integers(1, 3)), T, N, int(rng.choice([64, 128])), P,
                       int(rng.integers(0, 1 << 30))))
@@ -91,9 +106,9 @@ def test_factored_random_shapes(B, H, T, N, d, P, seed):
 def _stacked_cases():
     """Non-causal chunks of npairs * 256 + rem rows (rem a multiple of 8,
     P * rem <= 128): every rank's last rem rows share one query tile."""
-    rng = np.random.default_rng(7770)
+    rng = np.random.default_rng(7770 + SEED)
     cases = []
-    for i in range(6):
+    for i in range(6 * SCALE):
         P = int(rng.choice([2, 3, 4, 5, 8]))
         rem = int(rng.choice([8, 16, 24, 32, 40, 48, 64]))
         if P * rem > 128:
