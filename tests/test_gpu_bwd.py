@@ -57,3 +57,26 @@ def test_ring_backward_matches_oracle(B, H, S, d, P, causal):
         err = np.max(np.abs(got - want))
         scale = np.max(np.abs(want))
         assert err <= 1e-2 * scale + 1e-3, f"{name}: max|d| = {err:.3e}, max|ref| = {scale:.3e}"
+
+
+def _random_cases():
+    """Seeded random ring shapes for the backward: P from 1 to 8, causal or
+    not, both head sizes, ragged chunks.  RA_FUZZ_SCALE / RA_FUZZ_SEED /
+    RA_FUZZ_SMAX widen them as in tests/test_gpu_fuzz.py."""
+    import os
+    scale = int(os.environ.get("RA_FUZZ_SCALE", "1"))
+    smax = int(os.environ.get("RA_FUZZ_SMAX", "2400"))
+    rng = np.random.default_rng(5150 + int(os.environ.get("RA_FUZZ_SEED", "0")))
+    cases = []
+    while len(cases) < 8 * scale:
+        P = int(rng.integers(1, 9))
+        causal = bool(rng.integers(0, 2))
+        unit = 2 * P if causal else P
+        S = unit * int(rng.integers(1, max(2, min(smax, 1600) // unit)))
+        cases.append((1, int(rng.integers(1, 3)), S, int(rng.choice([64, 128])), P, causal))
+    return cases
+
+
+@pytest.mark.parametrize("B,H,S,d,P,causal", _random_cases())
+def test_ring_backward_random_shapes(B, H, S, d, P, causal):
+    test_ring_backward_matches_oracle(B, H, S, d, P, causal)
