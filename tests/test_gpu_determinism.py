@@ -54,6 +54,24 @@ def test_overlapped_ring_and_backward_are_deterministic():
     _same_every_time(lambda: ra.ring_attn_bwd(q, k, v, o, lse, do, P))
 
 
+@pytest.mark.parametrize("B,H,S,d,P,causal", [(1, 8, 4096, 128, 4, False), (1, 4, 4096, 64, 2, True),
+                                              (2, 3, 1320, 128, 5, False)])
+def test_overlap_exchange_forms_are_bit_identical(B, H, S, d, P, causal):
+    """The ring sends done by the step launches and the same sends as device
+    copies on a comm stream move identical bytes into identical buffers, and
+    the step launches compute the same partials: the outputs must agree bit
+    for bit (a copy landing late or in the wrong place would show)."""
+    g = torch.Generator(device="cuda").manual_seed(11 + P)
+    q, k, v = (_rnd(g, B, H, S, d) for _ in range(3))
+    if causal:
+        q, k, v = (ra.ra_cp_shard(x, P, 1) for x in (q, k, v))
+    o1, l1 = ra.ring_attn_fwd_overlap(q, k, v, P, causal=causal, comm_stream=torch.cuda.Stream())
+    o2, l2 = ra.ring_attn_fwd_overlap(q, k, v, P, causal=causal)
+    torch.cuda.synchronize()
+    assert ra.ra_get_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 @pytest.mark.parametrize("causal,d,H,S", [(True, 64, 4, 4096), (False, 128, 4, 4096),
                                          (True, 64, 18, 2048), (False, 128, 18, 2048)])
 def test_split_units_are_deterministic(causal, d, H, S):
